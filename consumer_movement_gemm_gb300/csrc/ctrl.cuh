@@ -1,0 +1,149 @@
+// ctrl.cuh -- control-plane layout, kernel parameter blocks and constants.
+//
+// The control plane (slots, counters, status) lives in its own allocation,
+// apart from the data plane, as the NVLink-atomics page recommends (section
+// 3.1: synchronisation metadata kept separate from data).  Every counter is
+// monotonic and never reset ("cross-GPU sync protocols on PCIe", section 2):
+// after the R-th call on a handle every slot holds R, every chunk counter
+// 64*R and every row-block counter 128*R.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+namespace tovl {
+
+constexpr int kChunkRows = 64;     // watermark granularity (section 4 of the sync-protocol page)
+constexpr int kBlockRows = 128;    // row-block gate = GEMM M tile (section 5)
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;      // 6 warps: TMA, MMA, 4 x epilogue (consumers) / copy warps (producers)
+constexpr int kMaxShards = 64;
+constexpr int kMaxExperts = 512;
+
+constexpr int kStageA = kTileM * kTileK * 2;      // 16 KB
+constexpr int kStageB = kTileK * kTileN * 2;      // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;    // 48 KB
+constexpr int kTmemCols = 512;                    // two 128x256 fp32 accumulators
+// dynamic shared memory: stages + barriers + 1 KB alignment slack
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+
+// Device status codes (mirror tovl.h).
+enum : int {
+    kOk = 0,
+    kErrInvalid = 1,
+    kErrUnsupported = 2,
+    kErrCuda = 3,
+    kErrTimeout = 4,
+    kErrOom = 5,
+};
+
+// Statistics slots (64-bit), only written when stats are enabled.
+enum : int {
+    kStatGatePolls = 0,      // acquire polls issued by consumer gates
+    kStatConsStartNs = 1,    // earliest consumer start (%globaltimer)
+    kStatConsEndNs = 2,      // latest consumer end
+    kStatProdStartNs = 3,    // earliest producer start
+    kStatProdEndNs = 4,      // latest producer end (all rows published)
+    kStatTimeouts = 5,
+    kNumStats = 8,
+};
+
+struct Ctrl {
+    int* slot;            // [n_chunk_cap]  chunk watermark slots (single writer per round)
+    int* cnt;             // [n_chunk_cap]  chunk arrival counters
+    int* rbcnt;           // [n_block_cap]  row-block arrival counters
+    int* status;          // [1] sticky error code
+    int* abort_seq;       // [1] highest sequence that gave up waiting
+    unsigned long long* stats;   // [kNumStats]
+    long long* pub_ns;    // [n_chunk_cap]  publish time of each chunk (copy sweep)
+    long long* obs_ns;    // [n_chunk_cap]  first observation time by a waiter
+    int n_chunk_cap;
+    int n_block_cap;
+};
+
+// Routing plan produced on the device for one dispatch round.
+struct Plan {
+    int* counts;          // [E]
+    int* off;             // [E+1] padded segment starts (internal copy)
+    int* prev_off;        // [E+1] previous round's layout (zero-padding decision)
+    int* seg_count;       // [n_seg][E] per-segment counts, then segment prefixes
+    int* local_rank;      // [T*k] rank of each pair inside its segment and expert
+    int* dst;             // [T*k] destination row of each pair
+    int* src_of_dst;      // [row cap] token of each destination row, -1 = padding
+    int* pad;             // [block cap] padding rows per block (counter seed)
+    int* blk_expert;      // [block cap]
+    int* meta;            // [4] m_pad, n_blocks, zero_padding, error
+};
+
+enum : int { kModeGather = 0, kModeDispatch = 1 };
+
+struct FusedParams {
+    CUtensorMap tmap_a;   // A: gathered / dispatched rows [rows][K] bf16, box 64 x 128, 128B swizzle
+    CUtensorMap tmap_b;   // B: weights [(E*)K][N] bf16 row-major (MN-major operand), box 64 x 64
+    int mode;
+    int M;                // gather: rows of the gathered buffer
+    int N, K;
+    int n_kb;             // K / 64
+    int n_nb;             // N / 256
+    int n_producers;
+    int n_consumers;
+    int gated;            // consumers wait on the protocol before loading A
+    int seq;
+    int gate_seq;         // sequence the consumer gates wait for (seq, unless a fault is injected)
+    long long timeout_ns; // bound of a gate wait on other CTAs
+    long long pipe_timeout_ns;  // bound of a wait on this CTA's own pipeline (outlasts a gate timeout)
+    int copy_mode;        // 0: 16-byte vector copies, 1: bulk async copies through shared memory
+    int stats;
+    int row_bytes;        // K * 2
+    // gather sources
+    const void* shard[kMaxShards];
+    int n_shards;
+    int rows_per_shard;
+    // dispatch sources
+    const void* x;
+    const int* src_of_dst;
+    const int* pad;
+    const int* blk_expert;
+    const int* meta;
+    // destinations
+    void* gathered;       // gathered / dispatched buffer
+    void* out;            // [rows][N] bf16
+    int out_rows;         // gather: M; dispatch: row capacity of out
+    Ctrl ctrl;
+};
+
+struct PlanParams {
+    const int* topk;      // [T*k]
+    int n_pairs;          // T*k
+    int k;
+    int E;
+    int n_seg;
+    int row_cap;          // rows available in the dispatched buffer
+    int block_cap;        // row-block counters available
+    int force_zero;       // host: buffer changed, re-zero padding rows
+    int* expert_offsets;  // caller-visible [E+1]
+    Plan plan;
+    int* status;
+};
+
+struct CopyParams {
+    const uint8_t* src;
+    uint8_t* dst;
+    const int* perm;      // dst row of each src row
+    long long n_rows;
+    int row_bytes;
+    int n_chunks;         // chunks touched by this copy
+    int gated;
+    int n_copiers;        // CTAs that copy; the remaining CTAs wait on slots
+    int seq;
+    long long timeout_ns;
+    long long pipe_timeout_ns;
+    int copy_mode;
+    int stamps;           // record publish / observe times
+    Ctrl ctrl;
+};
+
+}  // namespace tovl

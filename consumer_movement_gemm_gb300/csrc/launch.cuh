@@ -1,0 +1,22 @@
+// launch.cuh -- internal launchers (one per kernel translation unit).
+#pragma once
+#include <cuda_runtime.h>
+#include "ctrl.cuh"
+
+namespace tovl {
+
+cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative);
+cudaError_t prepare_fused();
+int fused_max_active_per_sm();
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t prepare_plan();
+
+cudaError_t launch_copy(const CopyParams& p, int n_waiters, cudaStream_t stream);
+cudaError_t prepare_copy();
+int copy_max_active_per_sm(int copy_mode);
+int copy_bulk_max_row_bytes();
+constexpr int kCopyWarpsPerCta = 16;
+constexpr int kWaiterChunksPerWarp = 64 * 32;
+
+}  // namespace tovl

@@ -1,0 +1,171 @@
+// plan.cu -- routing plan for dispatch rounds.
+//
+// The notify stage of the DeepEP FIFO-pipeline page counts tokens per expert
+// before the data moves; here the count also fixes every destination row.
+// Rows of one expert are laid out in ascending (token, k) order, so the
+// dispatched buffer depends on the routing alone (atomic slot claims would
+// make the order, and hence the buffer, nondeterministic).  Each expert's
+// segment is padded to a multiple of 128 rows; the padding count of a block
+// is the seed its arrival counter receives ("cross-GPU sync protocols on
+// PCIe", section 5).
+//
+//   plan_count     one CTA per 1024 routed pairs: per-warp match_any ranks,
+//                  per-segment per-expert counts and in-segment ranks
+//   plan_finalize  one CTA: per-expert prefix over segments, padded offsets,
+//                  block -> expert / padding tables, destination rows and the
+//                  inverse map (token of each destination row)
+#include <cuda_runtime.h>
+#include "ctrl.cuh"
+#include "ptx.cuh"
+#include "launch.cuh"
+
+namespace tovl {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanWarps = kPlanThreads / 32;
+
+
+__global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const PlanParams p)
+{
+    extern __shared__ int wcnt[];               // [kPlanWarps][E]
+    const int tid = threadIdx.x;
+    const int warp = tid / 32;
+    const int lane = tid % 32;
+    for (int i = tid; i < kPlanWarps * p.E; i += kPlanThreads) wcnt[i] = 0;
+    __syncthreads();
+    const int i = blockIdx.x * kPlanThreads + tid;
+    int e = -1;
+    if (i < p.n_pairs) {
+        e = p.topk[i];
+        if (e < 0 || e >= p.E) {
+            ptx::atom_cas_relaxed_gpu(p.status, kOk, kErrInvalid);
+            p.plan.meta[3] = 1;
+            e = -1;
+        }
+    }
+    // lanes routed to the same expert; rank = earlier lanes with that expert
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank_in_warp == 0) wcnt[warp * p.E + e] = __popc(same);
+    __syncthreads();
+    // exclusive scan over warps, per expert; segment totals to global
+    for (int x = tid; x < p.E; x += kPlanThreads) {
+        int run = 0;
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const int v = wcnt[w * p.E + x];
+            wcnt[w * p.E + x] = run;
+            run += v;
+        }
+        p.plan.seg_count[blockIdx.x * p.E + x] = run;
+    }
+    __syncthreads();
+    if (i < p.n_pairs) p.plan.local_rank[i] = (e >= 0) ? wcnt[warp * p.E + e] + rank_in_warp : 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanParams p)
+{
+    extern __shared__ int sm[];
+    int* s_off = sm;                // [E+1]
+    int* s_cnt = sm + p.E + 1;      // [E]
+    __shared__ int s_zero;
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    const int* meta_in = p.plan.meta;
+    if (tid == 0) {
+        s_zero = p.force_zero;
+        s_bad = meta_in[3];
+    }
+    // per-expert prefix over segments (becomes each segment's base rank)
+    for (int e = tid; e < p.E; e += kPlanThreads) {
+        int run = 0;
+        for (int s = 0; s < p.n_seg; ++s) {
+            const int v = p.plan.seg_count[s * p.E + e];
+            p.plan.seg_count[s * p.E + e] = run;
+            run += v;
+        }
+        s_cnt[e] = run;
+        p.plan.counts[e] = run;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        s_off[0] = 0;
+        for (int e = 0; e < p.E; ++e) {
+            run += (s_cnt[e] + kBlockRows - 1) / kBlockRows * kBlockRows;
+            s_off[e + 1] = run;
+        }
+        if (run > p.row_cap || run / kBlockRows > p.block_cap) s_bad = 1;
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    if (bad) {
+        if (tid == 0) {
+            ptx::atom_cas_relaxed_gpu(p.status, kOk, kErrInvalid);
+            p.plan.meta[0] = 0;
+            p.plan.meta[1] = 0;
+            p.plan.meta[2] = 0;
+            p.plan.meta[3] = 0;
+        }
+        for (int e = tid; e <= p.E; e += kPlanThreads) p.expert_offsets[e] = 0;
+        return;
+    }
+    // layout change decides whether padding rows must be re-zeroed
+    for (int e = tid; e <= p.E; e += kPlanThreads) {
+        if (p.plan.prev_off[e] != s_off[e]) s_zero = 1;   // benign race: every writer stores 1
+    }
+    __syncthreads();
+    for (int e = tid; e <= p.E; e += kPlanThreads) {
+        p.plan.off[e] = s_off[e];
+        p.plan.prev_off[e] = s_off[e];
+        p.expert_offsets[e] = s_off[e];
+    }
+    const int m_pad = s_off[p.E];
+    if (tid == 0) {
+        p.plan.meta[0] = m_pad;
+        p.plan.meta[1] = m_pad / kBlockRows;
+        p.plan.meta[2] = s_zero;
+        p.plan.meta[3] = 0;
+    }
+    // block tables and padding rows of each expert segment
+    for (int e = tid; e < p.E; e += kPlanThreads) {
+        const int b0 = s_off[e] / kBlockRows, b1 = s_off[e + 1] / kBlockRows;
+        for (int b = b0; b < b1; ++b) {
+            p.plan.blk_expert[b] = e;
+            p.plan.pad[b] = (b == b1 - 1) ? (s_off[e + 1] - s_off[e] - s_cnt[e]) : 0;
+        }
+        for (int r = s_off[e] + s_cnt[e]; r < s_off[e + 1]; ++r) p.plan.src_of_dst[r] = -1;
+    }
+    // destination row of every pair and the inverse map
+    for (int i = tid; i < p.n_pairs; i += kPlanThreads) {
+        const int e = p.topk[i];
+        const int seg = i / kPlanThreads;
+        const int d = s_off[e] + p.plan.seg_count[seg * p.E + e] + p.plan.local_rank[i];
+        p.plan.dst[i] = d;
+        p.plan.src_of_dst[d] = i / p.k;
+    }
+}
+
+}  // namespace tovl
+
+namespace tovl {
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream)
+{
+    const size_t sm_count = static_cast<size_t>(kPlanWarps) * p.E * sizeof(int);
+    const size_t sm_fin = static_cast<size_t>(2 * p.E + 1) * sizeof(int);
+    if (p.n_seg > 0) {
+        plan_count_kernel<<<p.n_seg, kPlanThreads, sm_count, stream>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    plan_finalize_kernel<<<1, kPlanThreads, sm_fin, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_plan()
+{
+    return cudaFuncSetAttribute(plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPlanWarps * kMaxExperts * static_cast<int>(sizeof(int)));
+}
+
+}  // namespace tovl

@@ -1,0 +1,689 @@
+// tovl_api.cu -- host implementation of the C ABI declared in include/tovl.h.
+//
+// Owns the control plane of a handle (slots, counters, status word, plan
+// scratch) and the per-handle sequence number; validates every argument on
+// the host; encodes TMA tensor maps; launches the kernels on the caller's
+// stream.  No device work runs here besides memsets at creation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "tovl.h"
+#include "ctrl.cuh"
+#include "launch.cuh"
+
+#define TOVL_API extern "C" __attribute__((visibility("default")))
+
+using namespace tovl;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct tovl_ctx {
+    tovl_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    int producers = 16;
+    int consumers = 0;
+    int copy_mode = 1;
+    int stats = 0;
+    long long timeout_ns = 2000000000LL;
+    int copy_ctas = 0;       // copy sweep copiers (0 = auto)
+    int copy_waiters = 0;    // copy sweep waiters (0 = auto)
+    int fault_gate_offset = 0;  // test hook: gates wait for seq + offset
+    long long seq = 0;
+    Ctrl ctrl{};
+    Plan plan{};
+    int max_seg = 0;
+    void* ctrl_mem = nullptr;    // one allocation for the control plane
+    void* plan_mem = nullptr;    // one allocation for plan scratch
+    cudaStream_t last_stream = nullptr;
+    const void* last_dispatched = nullptr;
+    int last_T = 0, last_k = 0, last_E = 0;
+    EncodeTiledFn encode = nullptr;
+    char last_error[256] = {0};
+};
+
+static int cuda_fail(tovl_ctx* h, cudaError_t e, const char* what)
+{
+    if (h) std::snprintf(h->last_error, sizeof h->last_error, "%s: %s", what, cudaGetErrorString(e));
+    return TOVL_ERR_CUDA;
+}
+
+static bool aligned16(const void* p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+static long long ceil_div(long long a, long long b)
+{
+    return (a + b - 1) / b;
+}
+
+TOVL_API void tovl_default_config(tovl_config* cfg, int device)
+{
+    if (!cfg) return;
+    std::memset(cfg, 0, sizeof *cfg);
+    cfg->device = device;
+    cfg->chunk_rows = kChunkRows;
+    cfg->gate_rows = kBlockRows;
+    cfg->producer_ctas = 0;
+    cfg->consumer_ctas = 0;
+    cfg->wait_timeout_ns = 0;
+    cfg->copy_mode = 1;
+    cfg->max_rows = 1 << 16;
+    cfg->max_pairs = 1 << 16;
+    cfg->max_experts = 64;
+}
+
+TOVL_API const char* tovl_error_string(int code)
+{
+    switch (code) {
+    case TOVL_OK: return "ok";
+    case TOVL_ERR_INVALID: return "invalid argument";
+    case TOVL_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case TOVL_ERR_CUDA: return "CUDA runtime error";
+    case TOVL_ERR_TIMEOUT: return "device wait timed out";
+    case TOVL_ERR_OOM: return "out of device memory";
+    default: return "unknown error";
+    }
+}
+
+TOVL_API const char* tovl_last_error(tovl_handle h)
+{
+    return h ? h->last_error : "";
+}
+
+TOVL_API long long tovl_dispatch_rows(int T, int k, int E)
+{
+    if (T < 0 || k < 0 || E < 0) return 0;
+    return ceil_div(static_cast<long long>(T) * k + static_cast<long long>(E) * (kBlockRows - 1), kBlockRows) *
+           kBlockRows;
+}
+
+static void free_all(tovl_ctx* h)
+{
+    if (h->ctrl_mem) cudaFree(h->ctrl_mem);
+    if (h->plan_mem) cudaFree(h->plan_mem);
+    h->ctrl_mem = h->plan_mem = nullptr;
+}
+
+// Bump allocator over one device allocation; every piece 256-byte aligned.
+struct Carve {
+    char* base;
+    size_t off;
+    template <class T>
+    T* take(size_t n)
+    {
+        off = (off + 255) & ~static_cast<size_t>(255);
+        T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+        off += n * sizeof(T);
+        return p;
+    }
+};
+
+static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks)
+{
+    ctrl.slot = c.take<int>(n_chunks);
+    ctrl.cnt = c.take<int>(n_chunks);
+    ctrl.rbcnt = c.take<int>(n_blocks);
+    ctrl.status = c.take<int>(1);
+    ctrl.abort_seq = c.take<int>(1);
+    ctrl.stats = c.take<unsigned long long>(kNumStats);
+    ctrl.pub_ns = c.take<long long>(n_chunks);
+    ctrl.obs_ns = c.take<long long>(n_chunks);
+    ctrl.n_chunk_cap = n_chunks;
+    ctrl.n_block_cap = n_blocks;
+}
+
+static void carve_plan(Carve& c, Plan& p, int E, int max_seg, int max_pairs, long long rows, int n_blocks)
+{
+    p.counts = c.take<int>(E);
+    p.off = c.take<int>(E + 1);
+    p.prev_off = c.take<int>(E + 1);
+    p.seg_count = c.take<int>(static_cast<size_t>(max_seg) * E);
+    p.local_rank = c.take<int>(max_pairs);
+    p.dst = c.take<int>(max_pairs);
+    p.src_of_dst = c.take<int>(rows);
+    p.pad = c.take<int>(n_blocks);
+    p.blk_expert = c.take<int>(n_blocks);
+    p.meta = c.take<int>(4);
+}
+
+TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
+{
+    if (!out) return TOVL_ERR_INVALID;
+    *out = nullptr;
+    if (!cfg_in) return TOVL_ERR_INVALID;
+    tovl_config cfg = *cfg_in;
+    if (cfg.chunk_rows == 0) cfg.chunk_rows = kChunkRows;
+    if (cfg.gate_rows == 0) cfg.gate_rows = kBlockRows;
+    if (cfg.chunk_rows != kChunkRows || cfg.gate_rows != kBlockRows) return TOVL_ERR_UNSUPPORTED;
+    if (cfg.max_rows < 1 || cfg.max_rows > (1LL << 30)) return TOVL_ERR_INVALID;
+    if (cfg.max_pairs < 0 || cfg.max_pairs > (1 << 28)) return TOVL_ERR_INVALID;
+    if (cfg.max_experts < 0 || cfg.max_experts > kMaxExperts) return TOVL_ERR_INVALID;
+    if (cfg.producer_ctas < 0 || cfg.consumer_ctas < 0 || cfg.wait_timeout_ns < 0) return TOVL_ERR_INVALID;
+    if (cfg.copy_mode != TOVL_COPY_VECTOR && cfg.copy_mode != TOVL_COPY_BULK) return TOVL_ERR_INVALID;
+
+    int n_dev = 0;
+    if (cudaGetDeviceCount(&n_dev) != cudaSuccess || n_dev == 0) {
+        cudaGetLastError();
+        return TOVL_ERR_UNSUPPORTED;
+    }
+    if (cfg.device < 0 || cfg.device >= n_dev) return TOVL_ERR_INVALID;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, cfg.device) != cudaSuccess) return TOVL_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return TOVL_ERR_UNSUPPORTED;
+
+    tovl_ctx* h = new (std::nothrow) tovl_ctx();
+    if (!h) return TOVL_ERR_OOM;
+    h->cfg = cfg;
+    h->device = cfg.device;
+    h->num_sms = prop.multiProcessorCount;
+    h->producers = cfg.producer_ctas ? cfg.producer_ctas : 16;
+    h->consumers = cfg.consumer_ctas;
+    h->copy_mode = cfg.copy_mode;
+    if (cfg.wait_timeout_ns) h->timeout_ns = cfg.wait_timeout_ns;
+
+    int prev_dev = 0;
+    cudaGetDevice(&prev_dev);
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return TOVL_ERR_CUDA;
+    }
+    int rc = TOVL_OK;
+    do {
+        if ((e = prepare_fused()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare fused"); break; }
+        if ((e = prepare_plan()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare plan"); break; }
+        if ((e = prepare_copy()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare copy"); break; }
+        if (fused_max_active_per_sm() < 1) { rc = TOVL_ERR_UNSUPPORTED; break; }
+
+        const int n_chunks = static_cast<int>(ceil_div(cfg.max_rows, kChunkRows));
+        const int n_blocks = static_cast<int>(ceil_div(cfg.max_rows, kBlockRows));
+        Carve sizing{nullptr, 0};
+        Ctrl tmp_ctrl{};
+        carve_ctrl(sizing, tmp_ctrl, n_chunks, n_blocks);
+        const size_t ctrl_bytes = sizing.off + 256;
+        if ((e = cudaMalloc(&h->ctrl_mem, ctrl_bytes)) != cudaSuccess) { rc = TOVL_ERR_OOM; cudaGetLastError(); break; }
+        if ((e = cudaMemset(h->ctrl_mem, 0, ctrl_bytes)) != cudaSuccess) { rc = cuda_fail(h, e, "memset"); break; }
+        Carve cc{static_cast<char*>(h->ctrl_mem), 0};
+        carve_ctrl(cc, h->ctrl, n_chunks, n_blocks);
+
+        const int E = cfg.max_experts > 0 ? cfg.max_experts : 1;
+        h->max_seg = static_cast<int>(ceil_div(cfg.max_pairs > 0 ? cfg.max_pairs : 1, 1024));
+        Carve psz{nullptr, 0};
+        Plan tmp_plan{};
+        carve_plan(psz, tmp_plan, E, h->max_seg, cfg.max_pairs > 0 ? cfg.max_pairs : 1, cfg.max_rows, n_blocks);
+        const size_t plan_bytes = psz.off + 256;
+        if ((e = cudaMalloc(&h->plan_mem, plan_bytes)) != cudaSuccess) { rc = TOVL_ERR_OOM; cudaGetLastError(); break; }
+        if ((e = cudaMemset(h->plan_mem, 0, plan_bytes)) != cudaSuccess) { rc = cuda_fail(h, e, "memset"); break; }
+        Carve pc{static_cast<char*>(h->plan_mem), 0};
+        carve_plan(pc, h->plan, E, h->max_seg, cfg.max_pairs > 0 ? cfg.max_pairs : 1, cfg.max_rows, n_blocks);
+
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+            rc = cuda_fail(h, e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled");
+            break;
+        }
+        h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) { rc = cuda_fail(h, e, "create sync"); break; }
+    } while (0);
+    if (rc != TOVL_OK) {
+        free_all(h);
+        delete h;
+        cudaSetDevice(prev_dev);
+        return rc;
+    }
+    cudaSetDevice(prev_dev);
+    *out = h;
+    return TOVL_OK;
+}
+
+TOVL_API int tovl_destroy(tovl_handle h)
+{
+    if (!h) return TOVL_OK;
+    int prev_dev = 0;
+    cudaGetDevice(&prev_dev);
+    cudaSetDevice(h->device);
+    if (h->last_stream) cudaStreamSynchronize(h->last_stream);
+    cudaDeviceSynchronize();
+    free_all(h);
+    cudaSetDevice(prev_dev);
+    delete h;
+    return TOVL_OK;
+}
+
+TOVL_API int tovl_num_sms(tovl_handle h)
+{
+    return h ? h->num_sms : 0;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// rows `stride` bytes apart; boxes of box_inner x box_outer, 128B swizzle,
+// out-of-range elements read as zero.
+static int encode_2d(tovl_ctx* h, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t stride, uint32_t box_inner, uint32_t box_outer)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(h->last_error, sizeof h->last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+        return TOVL_ERR_INVALID;
+    }
+    return TOVL_OK;
+}
+
+// Waits inside one CTA's own pipeline depend on its gate waits, so their
+// bound must outlast a gate timeout.
+static long long pipe_timeout(const tovl_ctx* h)
+{
+    return 4 * h->timeout_ns + 100000000LL;
+}
+
+static void base_params(tovl_ctx* h, FusedParams& p)
+{
+    std::memset(&p, 0, sizeof p);
+    p.timeout_ns = h->timeout_ns;
+    p.pipe_timeout_ns = pipe_timeout(h);
+    p.copy_mode = h->copy_mode;
+    p.stats = h->stats;
+    p.ctrl = h->ctrl;
+}
+
+static void split_ctas(tovl_ctx* h, int& P, int& C)
+{
+    P = h->producers;
+    if (P > h->num_sms - 1) P = h->num_sms - 1;
+    C = h->consumers ? h->consumers : h->num_sms - P;
+    if (C > h->num_sms - P) C = h->num_sms - P;
+    if (C < 1) C = 1;
+}
+
+static int reset_stats(tovl_ctx* h, cudaStream_t s)
+{
+    if (!h->stats) return TOVL_OK;
+    // min slots start at all-ones, the others at zero
+    cudaError_t e = cudaMemsetAsync(h->ctrl.stats, 0, kNumStats * sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->ctrl.stats + kStatConsStartNs, 0xff, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->ctrl.stats + kStatProdStartNs, 0xff, sizeof(unsigned long long), s);
+    return e == cudaSuccess ? TOVL_OK : cuda_fail(h, e, "stats reset");
+}
+
+struct DeviceGuard {
+    int prev = 0;
+    explicit DeviceGuard(int dev)
+    {
+        cudaGetDevice(&prev);
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() { cudaSetDevice(prev); }
+};
+
+// Shared validation of the gather shapes.
+static int check_gather(tovl_ctx* h, const void* const* shards, int S, int R, int K)
+{
+    if (!shards || S < 1 || S > kMaxShards || R < 1 || K < kTileK || K % kTileK) return TOVL_ERR_INVALID;
+    if (static_cast<long long>(S) * R > h->cfg.max_rows) return TOVL_ERR_INVALID;
+    for (int s = 0; s < S; ++s)
+        if (!shards[s] || !aligned16(shards[s])) return TOVL_ERR_INVALID;
+    if (h->copy_mode == TOVL_COPY_BULK && K * 2 > 32768) return TOVL_ERR_UNSUPPORTED;
+    return TOVL_OK;
+}
+
+// flags: 1 = producers, 2 = consumers, 4 = gated
+static int run_gather(tovl_handle h, const void* const* shards, int S, int R, int K, const void* W, int N,
+                      void* gathered, const void* A, void* out, cudaStream_t stream, int flags)
+{
+    const int M = S * R;
+    FusedParams p;
+    base_params(h, p);
+    p.mode = kModeGather;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.n_kb = K / kTileK;
+    p.n_nb = N / kTileN;
+    p.row_bytes = K * 2;
+    int P, C;
+    split_ctas(h, P, C);
+    p.n_producers = (flags & 1) ? P : 0;
+    p.n_consumers = (flags & 2) ? C : 0;
+    p.gated = (flags & 4) ? 1 : 0;
+    p.n_shards = S;
+    p.rows_per_shard = R;
+    for (int s = 0; s < S; ++s) p.shard[s] = shards ? shards[s] : nullptr;
+    p.gathered = gathered;
+    p.out = out;
+    p.out_rows = M;
+    int rc;
+    if (flags & 2) {
+        if ((rc = encode_2d(h, &p.tmap_a, A, K, M, static_cast<uint64_t>(K) * 2, kTileK, kTileM)) != TOVL_OK) return rc;
+        if ((rc = encode_2d(h, &p.tmap_b, W, N, K, static_cast<uint64_t>(N) * 2, 64, kTileK)) != TOVL_OK) return rc;
+    }
+    const bool round = (flags & 1) != 0;
+    if (round) p.seq = static_cast<int>(h->seq + 1);
+    else p.seq = static_cast<int>(h->seq);
+    p.gate_seq = p.seq + h->fault_gate_offset;
+    if ((rc = reset_stats(h, stream)) != TOVL_OK) return rc;
+    const cudaError_t e = launch_fused(p, stream, (flags & 4) != 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
+    if (round) h->seq += 1;
+    h->last_stream = stream;
+    return TOVL_OK;
+}
+
+TOVL_API int tovl_gather_gemm(tovl_handle h, const void* const* shards, int num_shards, int rows_per_shard, int K,
+                              const void* W, int N, void* gathered, void* out, void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    int rc = check_gather(h, shards, num_shards, rows_per_shard, K);
+    if (rc != TOVL_OK) return rc;
+    if (!W || !gathered || !out || !aligned16(W) || !aligned16(gathered) || !aligned16(out)) return TOVL_ERR_INVALID;
+    if (N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    return run_gather(h, shards, num_shards, rows_per_shard, K, W, N, gathered, gathered, out,
+                      static_cast<cudaStream_t>(stream), 1 | 2 | 4);
+}
+
+TOVL_API int tovl_copy_only(tovl_handle h, const void* const* shards, int num_shards, int rows_per_shard, int K,
+                            void* gathered, void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    int rc = check_gather(h, shards, num_shards, rows_per_shard, K);
+    if (rc != TOVL_OK) return rc;
+    if (!gathered || !aligned16(gathered)) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    return run_gather(h, shards, num_shards, rows_per_shard, K, nullptr, kTileN, gathered, nullptr, nullptr,
+                      static_cast<cudaStream_t>(stream), 1);
+}
+
+TOVL_API int tovl_gemm_only(tovl_handle h, const void* A, int M, int K, const void* W, int N, void* out, void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (!A || !W || !out || !aligned16(A) || !aligned16(W) || !aligned16(out)) return TOVL_ERR_INVALID;
+    if (M < 1 || K < kTileK || K % kTileK) return TOVL_ERR_INVALID;
+    if (N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    return run_gather(h, nullptr, 1, M, K, W, N, nullptr, A, out, static_cast<cudaStream_t>(stream), 2);
+}
+
+TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const int* topk_idx, int k, int E,
+                                        const void* W, int N, void* dispatched, int* expert_offsets, void* out,
+                                        void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (!x || !topk_idx || !W || !dispatched || !expert_offsets || !out) return TOVL_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(dispatched) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        return TOVL_ERR_INVALID;
+    if (T < 0 || k < 1 || E < 1 || E > h->cfg.max_experts || E > kMaxExperts) return TOVL_ERR_INVALID;
+    if (H < kTileK || H % kTileK) return TOVL_ERR_INVALID;
+    if (N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
+    const long long pairs = static_cast<long long>(T) * k;
+    if (pairs > h->cfg.max_pairs) return TOVL_ERR_INVALID;
+    const long long rows = tovl_dispatch_rows(T, k, E);
+    if (rows > h->cfg.max_rows) return TOVL_ERR_INVALID;
+    if (h->copy_mode == TOVL_COPY_BULK && H * 2 > 32768) return TOVL_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    PlanParams pp;
+    std::memset(&pp, 0, sizeof pp);
+    pp.topk = topk_idx;
+    pp.n_pairs = static_cast<int>(pairs);
+    pp.k = k;
+    pp.E = E;
+    pp.n_seg = static_cast<int>(ceil_div(pairs, 1024));
+    pp.row_cap = static_cast<int>(rows);
+    pp.block_cap = h->ctrl.n_block_cap;
+    pp.force_zero = (dispatched != h->last_dispatched) ? 1 : 0;
+    pp.expert_offsets = expert_offsets;
+    pp.plan = h->plan;
+    pp.status = h->ctrl.status;
+    cudaError_t e = launch_plan(pp, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan launch");
+
+    FusedParams p;
+    base_params(h, p);
+    p.mode = kModeDispatch;
+    p.M = static_cast<int>(rows);
+    p.N = N;
+    p.K = H;
+    p.n_kb = H / kTileK;
+    p.n_nb = N / kTileN;
+    p.row_bytes = H * 2;
+    int P, C;
+    split_ctas(h, P, C);
+    p.n_producers = P;
+    p.n_consumers = C;
+    p.gated = 1;
+    p.x = x;
+    p.src_of_dst = h->plan.src_of_dst;
+    p.pad = h->plan.pad;
+    p.blk_expert = h->plan.blk_expert;
+    p.meta = h->plan.meta;
+    p.gathered = dispatched;
+    p.out = out;
+    p.out_rows = static_cast<int>(rows);
+    int rc;
+    if ((rc = encode_2d(h, &p.tmap_a, dispatched, H, rows, static_cast<uint64_t>(H) * 2, kTileK, kTileM)) != TOVL_OK)
+        return rc;
+    if ((rc = encode_2d(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(N) * 2, 64, kTileK)) !=
+        TOVL_OK)
+        return rc;
+    p.seq = static_cast<int>(h->seq + 1);
+    p.gate_seq = p.seq + h->fault_gate_offset;
+    if ((rc = reset_stats(h, s)) != TOVL_OK) return rc;
+    e = launch_fused(p, s, true);
+    if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
+    h->seq += 1;
+    h->last_stream = s;
+    h->last_dispatched = dispatched;
+    h->last_T = T;
+    h->last_k = k;
+    h->last_E = E;
+    return TOVL_OK;
+}
+
+TOVL_API int tovl_gated_copy(tovl_handle h, const void* src, void* dst, long long n_rows, int row_bytes, const int* perm,
+                             int gated, int stamps, void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (!src || !dst || !perm || !aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(perm) & 3u))
+        return TOVL_ERR_INVALID;
+    if (n_rows < 1 || n_rows > h->cfg.max_rows || row_bytes < 16 || row_bytes % 16) return TOVL_ERR_INVALID;
+    if (h->copy_mode == TOVL_COPY_BULK && row_bytes > copy_bulk_max_row_bytes()) return TOVL_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    CopyParams p;
+    std::memset(&p, 0, sizeof p);
+    p.src = static_cast<const uint8_t*>(src);
+    p.dst = static_cast<uint8_t*>(dst);
+    p.perm = perm;
+    p.n_rows = n_rows;
+    p.row_bytes = row_bytes;
+    p.n_chunks = static_cast<int>(ceil_div(n_rows, kChunkRows));
+    p.gated = gated ? 1 : 0;
+    p.timeout_ns = h->timeout_ns;
+    p.pipe_timeout_ns = pipe_timeout(h);
+    p.copy_mode = h->copy_mode;
+    p.stamps = (gated && stamps) ? 1 : 0;
+    p.ctrl = h->ctrl;
+    const int per_sm = copy_max_active_per_sm(p.copy_mode);
+    if (per_sm < 1) return TOVL_ERR_UNSUPPORTED;
+    int waiters = 0;
+    if (p.gated) {
+        const long long per_cta = static_cast<long long>(kCopyWarpsPerCta) * kWaiterChunksPerWarp;
+        waiters = h->copy_waiters ? h->copy_waiters : static_cast<int>(ceil_div(p.n_chunks, per_cta));
+        if (static_cast<long long>(waiters) * per_cta < p.n_chunks) return TOVL_ERR_INVALID;
+    }
+    int copiers = h->copy_ctas ? h->copy_ctas : h->num_sms * per_sm - waiters;
+    if (copiers + waiters > h->num_sms * per_sm) copiers = h->num_sms * per_sm - waiters;
+    if (copiers < 1) return TOVL_ERR_INVALID;
+    p.n_copiers = copiers;
+    p.seq = static_cast<int>(p.gated ? h->seq + 1 : h->seq);
+    const cudaError_t e = launch_copy(p, waiters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "copy launch");
+    if (p.gated) h->seq += 1;
+    h->last_stream = static_cast<cudaStream_t>(stream);
+    return TOVL_OK;
+}
+
+static int sync_last(tovl_ctx* h)
+{
+    cudaError_t e = h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e == cudaSuccess ? TOVL_OK : cuda_fail(h, e, "synchronize");
+}
+
+TOVL_API int tovl_sync_status(tovl_handle h)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    if (rc != TOVL_OK) return rc;
+    int st = 0;
+    cudaError_t e = cudaMemcpy(&st, h->ctrl.status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+    if (st != 0) {
+        e = cudaMemset(h->ctrl.status, 0, sizeof st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
+    }
+    return st;
+}
+
+TOVL_API int tovl_ctrl_sizes(tovl_handle h, int* n_chunks, int* n_blocks)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (n_chunks) *n_chunks = h->ctrl.n_chunk_cap;
+    if (n_blocks) *n_blocks = h->ctrl.n_block_cap;
+    return TOVL_OK;
+}
+
+static int d2h(tovl_ctx* h, void* dst, const void* src, size_t bytes)
+{
+    if (!dst || !bytes) return TOVL_OK;
+    const cudaError_t e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? TOVL_OK : cuda_fail(h, e, "copy to host");
+}
+
+TOVL_API int tovl_read_ctrl(tovl_handle h, int* slots, int* cnts, int* rbcnts, long long* seq)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    const size_t nc = static_cast<size_t>(h->ctrl.n_chunk_cap) * sizeof(int);
+    const size_t nb = static_cast<size_t>(h->ctrl.n_block_cap) * sizeof(int);
+    if (rc == TOVL_OK) rc = d2h(h, slots, h->ctrl.slot, nc);
+    if (rc == TOVL_OK) rc = d2h(h, cnts, h->ctrl.cnt, nc);
+    if (rc == TOVL_OK) rc = d2h(h, rbcnts, h->ctrl.rbcnt, nb);
+    if (rc == TOVL_OK && seq) *seq = h->seq;
+    return rc;
+}
+
+TOVL_API int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* pad, int* blk_expert,
+                            int* m_pad)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    int meta[4] = {0, 0, 0, 0};
+    if (rc == TOVL_OK) rc = d2h(h, meta, h->plan.meta, sizeof meta);
+    const size_t pairs = static_cast<size_t>(h->last_T) * h->last_k;
+    if (rc == TOVL_OK) rc = d2h(h, counts, h->plan.counts, static_cast<size_t>(h->last_E) * sizeof(int));
+    if (rc == TOVL_OK) rc = d2h(h, dst, h->plan.dst, pairs * sizeof(int));
+    if (rc == TOVL_OK) rc = d2h(h, src_of_dst, h->plan.src_of_dst, static_cast<size_t>(meta[0]) * sizeof(int));
+    if (rc == TOVL_OK) rc = d2h(h, pad, h->plan.pad, static_cast<size_t>(meta[1]) * sizeof(int));
+    if (rc == TOVL_OK) rc = d2h(h, blk_expert, h->plan.blk_expert, static_cast<size_t>(meta[1]) * sizeof(int));
+    if (rc == TOVL_OK && m_pad) *m_pad = meta[0];
+    return rc;
+}
+
+TOVL_API int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n)
+{
+    if (!h || !stats || n < 0) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    if (n > kNumStats) n = kNumStats;
+    if (rc == TOVL_OK) rc = d2h(h, stats, h->ctrl.stats, static_cast<size_t>(n) * sizeof(unsigned long long));
+    return rc;
+}
+
+TOVL_API int tovl_read_latency(tovl_handle h, long long* pub_ns, long long* obs_ns, int n)
+{
+    if (!h || n < 0 || n > h->ctrl.n_chunk_cap) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    if (rc == TOVL_OK) rc = d2h(h, pub_ns, h->ctrl.pub_ns, static_cast<size_t>(n) * sizeof(long long));
+    if (rc == TOVL_OK) rc = d2h(h, obs_ns, h->ctrl.obs_ns, static_cast<size_t>(n) * sizeof(long long));
+    return rc;
+}
+
+TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    switch (option) {
+    case 1:
+        if (value < 1 || value >= h->num_sms) return TOVL_ERR_INVALID;
+        h->producers = static_cast<int>(value);
+        return TOVL_OK;
+    case 2:
+        if (value < 0 || value > h->num_sms) return TOVL_ERR_INVALID;
+        h->consumers = static_cast<int>(value);
+        return TOVL_OK;
+    case 3:
+        if (value != TOVL_COPY_VECTOR && value != TOVL_COPY_BULK) return TOVL_ERR_INVALID;
+        h->copy_mode = static_cast<int>(value);
+        return TOVL_OK;
+    case 4:
+        h->stats = value ? 1 : 0;
+        return TOVL_OK;
+    case 5:
+        if (value < 1000) return TOVL_ERR_INVALID;
+        h->timeout_ns = value;
+        return TOVL_OK;
+    case 6:
+        if (value < 0) return TOVL_ERR_INVALID;
+        h->copy_ctas = static_cast<int>(value);
+        return TOVL_OK;
+    case 7:
+        if (value < 0) return TOVL_ERR_INVALID;
+        h->copy_waiters = static_cast<int>(value);
+        return TOVL_OK;
+    case 8:
+        if (value < 0 || value > 1000) return TOVL_ERR_INVALID;
+        h->fault_gate_offset = static_cast<int>(value);
+        return TOVL_OK;
+    default:
+        return TOVL_ERR_INVALID;
+    }
+}
+
+TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
+{
+    if (!h || !value) return TOVL_ERR_INVALID;
+    int P, C;
+    split_ctas(h, P, C);
+    switch (option) {
+    case 1: *value = P; return TOVL_OK;
+    case 2: *value = C; return TOVL_OK;
+    case 3: *value = h->copy_mode; return TOVL_OK;
+    case 4: *value = h->stats; return TOVL_OK;
+    case 5: *value = h->timeout_ns; return TOVL_OK;
+    case 6: *value = h->copy_ctas; return TOVL_OK;
+    case 7: *value = h->copy_waiters; return TOVL_OK;
+    case 8: *value = h->fault_gate_offset; return TOVL_OK;
+    default: return TOVL_ERR_INVALID;
+    }
+}

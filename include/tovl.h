@@ -1,0 +1,208 @@
+/*
+ * tovl.h -- C ABI of the tovl library: token-row movement fused with a bf16
+ * tensor-core GEMM on one NVIDIA GB300 (sm_103a).
+ *
+ * The method: producer CTAs move token rows into one gathered buffer while
+ * consumer CTAs run a GEMM that starts on each 128-row block as soon as its
+ * rows are complete.  Completion follows the single-writer slot protocol of
+ * the Astro Bear page "Fused compute/communication operators (4): cross-GPU
+ * sync protocols on PCIe -- single writer, election and watermarks":
+ *   section 2  slots hold monotonically increasing sequence numbers that are
+ *              never reset; round k waits for a value >= k;
+ *   section 3  many writers are counted with a local acq_rel atomic and the
+ *              last arrival is elected to publish with a release store;
+ *   section 4  one watermark slot per 64-row chunk;
+ *   section 5  row-block counters take release reductions and are pre-seeded
+ *              with the padding count, so real arrivals reach 128 exactly.
+ * The "ranks" of the pages are logical shards held in this GPU's memory; the
+ * library uses no peer memory and no collectives.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the
+ *     handle's GPU, 16-byte aligned; host pointers are ordinary host memory.
+ *   - bf16 tensors are row-major with unit stride in the last dimension.
+ *   - The caller owns every buffer and stream; the handle owns only its
+ *     control plane (counters, slots, status word, plan scratch) and its
+ *     sequence number.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous; one call is one protocol round.  Calls on one handle must
+ *     be issued from one host thread, in order, on one stream.
+ *   - Return value: TOVL_OK, or an error code from tovl_status.  Argument
+ *     errors are detected on the host before anything is enqueued and leave
+ *     the handle unchanged.  Errors found on the device (a wait that timed
+ *     out, an expert id out of range) are sticky in the handle's status word
+ *     and read with tovl_sync_status(); device code never traps.
+ *   - There is no CPU fallback: on a machine without a compute-capability
+ *     10.3 GPU, tovl_create returns TOVL_ERR_UNSUPPORTED.
+ */
+#ifndef TOVL_H
+#define TOVL_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tovl_ctx* tovl_handle;
+
+typedef enum {
+    TOVL_OK = 0,
+    TOVL_ERR_INVALID = 1,      /* bad argument, shape, alignment or routing */
+    TOVL_ERR_UNSUPPORTED = 2,  /* shape or device the kernels do not support */
+    TOVL_ERR_CUDA = 3,         /* a CUDA runtime call failed; see tovl_last_error */
+    TOVL_ERR_TIMEOUT = 4,      /* a device wait gave up (sticky, from tovl_sync_status) */
+    TOVL_ERR_OOM = 5           /* device allocation failed in tovl_create */
+} tovl_status;
+
+/* Row-copy mechanism of the producers. */
+typedef enum {
+    TOVL_COPY_VECTOR = 0,      /* 16-byte vector loads/stores by warps */
+    TOVL_COPY_BULK = 1         /* bulk asynchronous copies through a shared-memory ring */
+} tovl_copy_mode;
+
+typedef struct {
+    int device;                /* CUDA device ordinal */
+    int chunk_rows;            /* watermark chunk; must be 64 (or 0 for 64) -- section 4 */
+    int gate_rows;             /* GEMM row-block gate; must be 128 (or 0 for 128) -- section 5 */
+    int producer_ctas;         /* P; 0 = 16 */
+    int consumer_ctas;         /* C; 0 = all remaining SMs */
+    long long wait_timeout_ns; /* bound of every device wait; 0 = 2 s */
+    int copy_mode;             /* tovl_copy_mode */
+    long long max_rows;        /* capacity in rows of gathered/dispatched buffers and copies */
+    int max_pairs;             /* largest T*k of a dispatch call */
+    int max_experts;           /* largest E of a dispatch call (<= 512) */
+} tovl_config;
+
+/* Fills `cfg` with defaults for `device`. */
+void tovl_default_config(tovl_config* cfg, int device);
+
+/* Creates a handle: validates `cfg`, checks the device (compute capability
+ * 10.3), allocates and zeroes the control plane (chunk slots and counters for
+ * max_rows/64 chunks, row-block counters for max_rows/128 blocks, status
+ * word, plan scratch).  Sequence number starts at 0.  On failure *out is
+ * NULL and nothing stays allocated. */
+int tovl_create(tovl_handle* out, const tovl_config* cfg);
+
+/* Frees the handle's device memory after synchronising its last stream.
+ * NULL is accepted.  The handle must not be used afterwards. */
+int tovl_destroy(tovl_handle h);
+
+/* All-gather of S logical shards followed by a GEMM (the tensor-parallel
+ * all-gather + GEMM of the platform page "know your platform", section 3,
+ * with the completion protocol of sections 2-5 of the sync page).
+ *   shards      host array of S device pointers; shard s is bf16 [R][K]
+ *   num_shards  S, 1..64
+ *   rows_per_shard R >= 1; M = S*R <= max_rows
+ *   K           multiple of 64
+ *   W           device, bf16 [K][N]
+ *   N           multiple of 256
+ *   gathered    device, bf16 [M][K]: receives G[s*R + i] = shard s row i
+ *   out         device, bf16 [M][N]: out = G x W, fp32 accumulation,
+ *               rounded to nearest even
+ * One round: producers copy every row and publish each 64-row chunk; each
+ * consumer tile waits for its chunks' slots to reach this round's sequence. */
+int tovl_gather_gemm(tovl_handle h, const void* const* shards, int num_shards, int rows_per_shard, int K,
+                     const void* W, int N, void* gathered, void* out, void* stream);
+
+/* Rows a dispatch buffer needs: T*k + E*127 rounded up to a multiple of 128. */
+long long tovl_dispatch_rows(int T, int k, int E);
+
+/* Dispatch scatter of top-k routed tokens into padded per-expert segments,
+ * followed by a grouped GEMM per expert (notify-stage counting of the DeepEP
+ * FIFO-pipeline page; row-block counters with padding seeds of section 5).
+ *   x           device, bf16 [T][H]
+ *   topk_idx    device, int32 [T][k]: expert of pair (t, j), each in [0, E)
+ *   H           multiple of 64 (the GEMM K)
+ *   W           device, bf16 [E][H][N], N multiple of 256
+ *   dispatched  device, bf16 [tovl_dispatch_rows(T,k,E)][H]: rows of expert e
+ *               occupy [off[e], off[e] + count[e]) in ascending (t, j) order;
+ *               the segment is padded with zero rows to a multiple of 128
+ *   expert_offsets device, int32 [E+1]: receives off[]; off[E] = padded total
+ *   out         device, bf16 [tovl_dispatch_rows(T,k,E)][N]: rows [off[e],
+ *               off[e+1]) = dispatched rows x W[e]; padding rows are zero;
+ *               rows >= off[E] are not written
+ * Padding rows of `dispatched` are re-zeroed whenever the segment layout or
+ * the buffer differs from the previous dispatch call on this handle.  An
+ * expert id outside [0, E) makes the round a no-op that sets
+ * TOVL_ERR_INVALID in the status word. */
+int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const int* topk_idx, int k, int E,
+                               const void* W, int N, void* dispatched, int* expert_offsets, void* out,
+                               void* stream);
+
+/* ---------------------------------------------------------------- controls
+ * The acceptance method of the platform page, section 5, compares the fused
+ * kernel with its parts run alone on the same SM counts. */
+
+/* GEMM-only control: the consumer CTAs of tovl_gather_gemm (same count C)
+ * with gates disabled, on an already filled A.  A: device bf16 [M][K],
+ * W: device bf16 [K][N], out: device bf16 [M][N].  Not a protocol round. */
+int tovl_gemm_only(tovl_handle h, const void* A, int M, int K, const void* W, int N, void* out, void* stream);
+
+/* Copy-only control: the producer CTAs of tovl_gather_gemm (same count P)
+ * with the full protocol and no consumers.  Arguments as tovl_gather_gemm.
+ * A protocol round. */
+int tovl_copy_only(tovl_handle h, const void* const* shards, int num_shards, int rows_per_shard, int K,
+                   void* gathered, void* stream);
+
+/* Permuted row copy dst[perm[i]] = src[i] over 64-row destination chunks.
+ *   src, dst    device, n_rows x row_bytes each (row_bytes multiple of 16)
+ *   perm        device, int32 [n_rows], a permutation of [0, n_rows)
+ *   gated       1: every row is an arrival on its destination chunk, the last
+ *               arrival publishes the chunk slot, waiter CTAs observe the
+ *               slots (a protocol round); 0: the same copy with no
+ *               protocol (not a round)
+ *   stamps      1: record publish and first-observe times per chunk
+ *               (read them with tovl_read_latency) */
+int tovl_gated_copy(tovl_handle h, const void* src, void* dst, long long n_rows, int row_bytes, const int* perm,
+                    int gated, int stamps, void* stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/* Synchronises the handle's last stream, returns the sticky device status
+ * (TOVL_OK if none) and clears it. */
+int tovl_sync_status(tovl_handle h);
+
+/* Number of chunk slots/counters and row-block counters of the handle. */
+int tovl_ctrl_sizes(tovl_handle h, int* n_chunks, int* n_blocks);
+
+/* Copies the control plane to host arrays (after synchronising): slots and
+ * cnts [n_chunks], rbcnts [n_blocks]; *seq = calls that were protocol rounds.
+ * Any pointer may be NULL. */
+int tovl_read_ctrl(tovl_handle h, int* slots, int* cnts, int* rbcnts, long long* seq);
+
+/* Copies the last dispatch round's plan to host arrays (after
+ * synchronising): counts [E], dst [T*k], src_of_dst [m_pad] (token of each
+ * row, -1 for padding), pad [m_pad/128], blk_expert [m_pad/128], *m_pad.
+ * Any pointer may be NULL. */
+int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* pad, int* blk_expert, int* m_pad);
+
+/* Options for sweeps: 1 = producer CTAs, 2 = consumer CTAs, 3 = copy mode,
+ * 4 = statistics on/off, 5 = wait timeout in ns, 6 = copy-sweep CTAs,
+ * 7 = copy-sweep waiter CTAs, 8 = fault injection for tests: consumer gates
+ * wait for sequence seq + value, which no producer publishes, so every gate
+ * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in
+ * the status word (0 = off). */
+int tovl_set_option(tovl_handle h, int option, long long value);
+int tovl_get_option(tovl_handle h, int option, long long* value);
+
+/* Statistics of the last call with statistics on: [0] gate polls,
+ * [1] earliest consumer start ns, [2] latest consumer end ns, [3] earliest
+ * producer start ns, [4] latest producer end ns. */
+int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n);
+
+/* Publish and first-observe %globaltimer stamps of the first n chunks of the
+ * last stamped tovl_gated_copy. */
+int tovl_read_latency(tovl_handle h, long long* pub_ns, long long* obs_ns, int n);
+
+/* Number of SMs of the handle's device. */
+int tovl_num_sms(tovl_handle h);
+
+const char* tovl_error_string(int code);
+
+/* Text of the last CUDA error seen by this handle ("" if none). */
+const char* tovl_last_error(tovl_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOVL_H */

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Buffers, plans and control-plane state must match bit for bit; GEMM outputs
+within |gpu - oracle| <= 2e-2 + 1e-2 |oracle| elementwise.  Inputs change
+every round (seed*1000 + round) so a stale read of an earlier round fails.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from consumer_movement_gemm_gb300 import tovl
+from tests.gpu_util import assert_close, bits
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from consumer_movement_gemm_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _handle(**kw):
+    kw.setdefault("max_rows", 1 << 14)
+    kw.setdefault("max_pairs", 1 << 14)
+    kw.setdefault("max_experts", 64)
+    kw.setdefault("wait_timeout_ns", 2_000_000_000)
+    return tovl.Handle(0, **kw)
+
+
+def _check_ctrl(h, R):
+    slots, cnts, rb, seq = h.read_ctrl()
+    o_slots, o_cnts, o_rb = oracle.ctrl_state(R, slots.size, rb.size)
+    assert seq == R
+    assert np.array_equal(slots, o_slots), "slots"
+    assert np.array_equal(cnts, o_cnts), "chunk counters"
+    assert np.array_equal(rb, o_rb), "row-block counters"
+
+
+# ------------------------------------------------------------------ GEMM alone
+@pytest.mark.parametrize("M,K,N", [(256, 256, 256), (128, 512, 512)])
+def test_gemm_only_identity_is_exact(M, K, N):
+    with _handle() as h:
+        A = workloads.bf16_normal((M, K), 1.0, 11, DEV)
+        W = torch.zeros(K, N, dtype=torch.bfloat16, device=DEV)
+        idx = torch.arange(min(K, N), device=DEV)
+        W[idx, idx] = 1.0
+        out = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=DEV)
+        h.gemm_only(A, W, out)
+        assert h.sync_status() == 0
+        want = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+        want[:, :min(K, N)] = A[:, :min(K, N)]
+        assert torch.equal(out, want)
+
+
+@pytest.mark.parametrize("M,K,N", [(384, 320, 512), (300, 192, 256), (1, 64, 256)])
+def test_gemm_only_matches_oracle(M, K, N):
+    with _handle() as h:
+        A = workloads.bf16_normal((M, K), 1 / math.sqrt(K), 12, DEV)
+        W = workloads.bf16_normal((K, N), 1 / math.sqrt(K), 13, DEV)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        h.gemm_only(A, W, out)
+        assert h.sync_status() == 0
+        assert_close(out, oracle.matmul_f32(bits(A), bits(W)), "gemm_only")
+
+
+# ------------------------------------------------------------------ gather + GEMM
+def _gather_round(h, cfg, seed):
+    X, W = workloads.gather_inputs(cfg, seed, DEV)
+    gathered = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=DEV)
+    h.gather_gemm(X, W, gathered, out)
+    return X, W, gathered, out
+
+
+@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
+def test_tiny_gather_gemm_three_rounds(copy_mode):
+    cfg = workloads.TINY
+    with _handle(copy_mode=copy_mode) as h:
+        for r in range(1, cfg.rounds + 1):
+            X, W, gathered, out = _gather_round(h, cfg, workloads.round_seed(cfg.seed, r))
+            assert h.sync_status() == 0
+            shards = [bits(X[s]) for s in range(cfg.shards)]
+            G = oracle.gather(shards)
+            assert np.array_equal(bits(gathered), G), f"gathered buffer, round {r}"
+            assert_close(out, oracle.matmul_f32(G, bits(W)), f"round {r}")
+            _check_ctrl(h, r)
+
+
+@pytest.mark.parametrize("S,R,K,N,P", [(3, 100, 192, 256, 4), (1, 64, 64, 512, 1), (5, 77, 128, 256, 32)])
+def test_gather_gemm_ragged(S, R, K, N, P):
+    cfg = workloads.GatherCfg("ragged", S, R, K, N, rounds=2)
+    with _handle(producer_ctas=P) as h:
+        for r in range(1, 3):
+            X, W, gathered, out = _gather_round(h, cfg, 100 + r)
+            assert h.sync_status() == 0
+            G = oracle.gather([bits(X[s]) for s in range(S)])
+            assert np.array_equal(bits(gathered), G)
+            assert_close(out, oracle.matmul_f32(G, bits(W)), "ragged")
+            _check_ctrl(h, r)
+
+
+@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
+def test_copy_only_control(copy_mode):
+    cfg = workloads.GatherCfg("copy", 4, 96, 256, 256, rounds=2)
+    with _handle(copy_mode=copy_mode) as h:
+        for r in range(1, 3):
+            X, _ = workloads.gather_inputs(cfg, r, DEV)
+            gathered = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device=DEV)
+            h.copy_only(X, gathered)
+            assert h.sync_status() == 0
+            assert np.array_equal(bits(gathered), oracle.gather([bits(X[s]) for s in range(4)]))
+            _check_ctrl(h, r)
+
+
+def test_timeout_is_reported_and_handle_recovers():
+    cfg = workloads.TINY
+    with _handle(wait_timeout_ns=5_000_000) as h:
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # gates wait for a sequence nobody publishes
+        _gather_round(h, cfg, 1)
+        assert h.sync_status() == tovl.TOVL_ERR_TIMEOUT
+        assert h.sync_status() == 0                        # the status word was cleared
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 0)
+        X, W, gathered, out = _gather_round(h, cfg, 2)
+        assert h.sync_status() == 0
+        G = oracle.gather([bits(X[s]) for s in range(cfg.shards)])
+        assert np.array_equal(bits(gathered), G)
+        assert_close(out, oracle.matmul_f32(G, bits(W)), "after timeout")
+        _check_ctrl(h, 2)
+
+
+# ------------------------------------------------------------------ dispatch + grouped GEMM
+def _dispatch_round(h, x, topk_np, W):
+    T, H = x.shape
+    k = topk_np.shape[1]
+    E, _, N = W.shape
+    rows = tovl.dispatch_rows(T, k, E)
+    topk = torch.from_numpy(topk_np).to(DEV)
+    dispatched = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device=DEV)   # non-zero garbage
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    out = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+    h.dispatch_grouped_gemm(x, topk, W, dispatched, offs, out)
+    return dispatched, offs, out
+
+
+def _check_dispatch(h, x, topk_np, W, dispatched, offs, out, R):
+    T, H = x.shape
+    k = topk_np.shape[1]
+    E = W.shape[0]
+    p = oracle.dispatch_plan(topk_np, E)
+    counts, dst, src, pad, blk, m_pad = h.read_plan(T, k, E)
+    assert m_pad == p.m_pad
+    assert np.array_equal(counts, p.counts)
+    assert np.array_equal(offs.cpu().numpy(), p.off)
+    assert np.array_equal(dst, p.dst)
+    assert np.array_equal(src, p.src)
+    assert np.array_equal(pad, p.pad)
+    assert np.array_equal(blk, p.blk_e)
+    D = oracle.dispatch(bits(x), p.dst, k, p.m_pad)
+    assert np.array_equal(bits(dispatched[:p.m_pad]), D), "dispatched buffer"
+    O = oracle.grouped_matmul_f32(D, bits(W), p.off)
+    assert_close(out[:p.m_pad], O, "grouped GEMM")
+    assert torch.count_nonzero(out[:p.m_pad][torch.from_numpy(p.src < 0).to(DEV)]) == 0
+    _check_ctrl(h, R)
+
+
+ROUTINGS = {
+    "uniform": lambda s: (workloads.uniform_topk(300, 2, 5, s), 5),
+    "zipf": lambda s: (workloads.zipf_topk(700, 4, 12, 1.2, s), 12),
+    "all_to_one": lambda s: (workloads.all_to_one_topk(260, 3, 1), 3),
+    "empty_expert": lambda s: (workloads.uniform_topk(200, 2, 4, s), 7),
+}
+
+
+@pytest.mark.parametrize("routing", list(ROUTINGS))
+@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
+def test_dispatch_grouped_gemm_small(routing, copy_mode):
+    H, N = 192, 256
+    with _handle(copy_mode=copy_mode) as h:
+        for r in range(1, 4):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(1, r))
+            T = topk_np.shape[0]
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 200 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 300 + r, DEV)
+            dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+            assert h.sync_status() == 0
+            _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
+
+
+def test_dispatch_bad_expert_id_is_a_noop_round():
+    H, N, E = 64, 256, 3
+    with _handle() as h:
+        topk_np = np.array([[0, 1], [2, 5]], np.int32)
+        x = workloads.bf16_normal((2, H), 1.0, 1, DEV)
+        W = workloads.bf16_normal((E, H, N), 1.0, 2, DEV)
+        _, offs, _ = _dispatch_round(h, x, topk_np, W)
+        assert h.sync_status() == tovl.TOVL_ERR_INVALID
+        assert torch.count_nonzero(offs) == 0
+        _check_ctrl(h, 1)
+        # the next round is normal
+        topk_np = np.array([[0, 1], [2, 1]], np.int32)
+        dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+        assert h.sync_status() == 0
+        _check_dispatch(h, x, topk_np, W, dispatched, offs, out, 2)
+
+
+# ------------------------------------------------------------------ gated copy
+@pytest.mark.parametrize("row_bytes", [256, 1024, 8192])
+@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK])
+def test_gated_copy_small(row_bytes, copy_mode):
+    n = 5000
+    with _handle(copy_mode=copy_mode, max_rows=n) as h:
+        for r in range(1, 3):
+            perm_np = workloads.permutation(n, r)
+            src = workloads.random_bytes(n, row_bytes, r, DEV)
+            dst = torch.zeros_like(src)
+            perm = torch.from_numpy(perm_np).to(DEV)
+            h.gated_copy(src, dst, perm, gated=True, stamps=True)
+            assert h.sync_status() == 0
+            assert np.array_equal(dst.cpu().numpy(), oracle.copy_perm(src.cpu().numpy(), perm_np))
+            _check_ctrl(h, r)
+            n_chunks = (n + 63) // 64
+            pub, obs = h.read_latency(n_chunks)
+            assert np.all(pub > 0) and np.all(obs >= pub)
+        # the ungated control copies the same way and is not a round
+        dst2 = torch.zeros_like(src)
+        h.gated_copy(src, dst2, perm, gated=False)
+        assert h.sync_status() == 0
+        assert torch.equal(dst2, dst)
+        _check_ctrl(h, 2)
