@@ -1,0 +1,505 @@
+"""Benchmark of the tovl hot path on GB300.
+
+Headline step: one tovl_gather_gemm call on the tensor-parallel all-gather +
+GEMM workload (4 logical shards x 768 rows, M=3072, K=N=4096, bf16), inputs
+resident in HBM, L2 flushed before every timed step (the buffers fit in L2).
+
+The JSON line also carries
+  acceptance  the platform page's trio: T_comp alone (GEMM-only control, same
+              consumer CTA count), T_comm alone (copy-only control, same
+              producer CTA count), T_total (fused); overlap efficiency and
+              compute interference
+  roofline    the fused kernel against the measured bf16 dense peak
+  e2e         the same metric through the C ABI with host buffers
+              (shards in, output out, pinned memory) inside the timed region
+  cpu_baseline the CPU oracle on a bounded sample on this host's cores
+  configs     the other workloads: dispatch + grouped GEMM (uniform and Zipf
+              routing) and the gated copy sweep (GB/s and signal latency)
+
+Multi-GPU: the path does not shard across GPUs (replicas only); with
+--gpus N each rank runs an independent replica and `value` sums the ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused gather+GEMM TFLOP/s & overlap eff. (1 GB300); gated row-copy HBM GB/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["tovl", "reference"], default="tovl")
+    ap.add_argument("--producers", type=int, default=0, help="producer CTAs (0 = library default)")
+    ap.add_argument("--copy-mode", type=int, default=1, help="copy mode of the gated copy sweep")
+    ap.add_argument("--k-slices", type=int, default=4, help="K-slices per chunk watermark")
+    ap.add_argument("--sweep", action="store_true", help="also sweep the producer CTA count")
+    ap.add_argument("--quick", action="store_true", help="skip the extra workloads")
+    ap.add_argument("--full", action="store_true", help="extra workloads at their full round counts")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- utilities
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def recorded_traffic(profile: str, source: str):
+    """DRAM bytes per launch from an ncu summary under profiles/, if it was
+    taken on the current kernel source (its sha256 is recorded there)."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source-sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram-bytes-per-launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
+    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+def dist_init(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def cpu_oracle_sample(cfg, seconds: float, seed: int = 0):
+    """Times the oracle (as it stands) on a bounded sample of the TP step:
+    the full gather plus the fp32 matmul of a subset of output rows."""
+    import numpy as np
+    import oracle
+    import workloads
+    X, W = workloads.gather_inputs(cfg, seed, "cpu")
+    shards = [workloads.bf16_bits(X[s]) for s in range(cfg.shards)]
+    Wb = workloads.bf16_bits(W)
+    t0 = time.perf_counter()
+    G = oracle.gather(shards)
+    t_gather = time.perf_counter() - t0
+    # calibrate the row count on a small sample, then run the bounded sample
+    rows = np.arange(8, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.matmul_rows_f32(G, Wb, rows)
+    per_row = (time.perf_counter() - t0) / rows.size
+    n = int(max(8, min(cfg.M, seconds / max(per_row, 1e-9))))
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(cfg.M, size=n, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.matmul_rows_f32(G, Wb, rows)
+    t_mm = time.perf_counter() - t0
+    step_s = t_gather + t_mm * cfg.M / n          # one whole step, extrapolated by rows
+    return {
+        "value": cfg.flops / step_s / 1e12,
+        "unit": "TFLOP/s",
+        "cores": oracle.num_threads(),
+        "kind": "oracle",
+        "sample": f"full gather + fp32 matmul of {n} of {cfg.M} output rows (K=N={cfg.K}); "
+                  f"{t_gather + t_mm:.1f} s of CPU time, step time extrapolated by rows",
+        "seconds": t_gather + t_mm,
+    }
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on this host's cores."""
+    import workloads
+    rank, world, _ = dist_init(args)
+    if rank != 0:
+        return
+    cfg = workloads.TP
+    per = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(cfg, per, seed=i)
+        if i >= args.warmup:
+            vals.append(r)
+    value = statistics.median(v["value"] for v in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": cfg.flops / (value * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "parallelism": "replicas only", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU legs
+class Timer:
+    """CUDA-event timing of single calls on one stream, L2 flushed before each."""
+
+    def __init__(self, stream):
+        import torch
+        self.torch = torch
+        self.stream = stream
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def time_calls(self, fn, n: int, flush: bool = True):
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(self.stream):
+            for a, b in evs:
+                if flush:
+                    self.flush.fill_(1)
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+        self.stream.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+
+def tp_setup(h, cfg, dev):
+    import torch
+    import workloads
+    X, W = workloads.gather_inputs(cfg, 0, dev)
+    gathered = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)
+    return X, W, gathered, out
+
+
+def acceptance(h, timer, cfg, X, W, gathered, out, n: int):
+    """T_comp alone, T_comm alone and T_total (median ms) plus the consumers'
+    span inside the fused kernel, from the kernel's own %globaltimer stamps."""
+    from consumer_movement_gemm_gb300 import tovl
+    t_total = statistics.median(timer.time_calls(lambda: h.gather_gemm(X, W, gathered, out), n))
+    t_comp = statistics.median(timer.time_calls(lambda: h.gemm_only(gathered, W, out), n))
+    t_comm = statistics.median(timer.time_calls(lambda: h.copy_only(X, gathered), n))
+    h.set_option(tovl.OPT_STATS, 1)
+    spans = []
+    for _ in range(min(n, 20)):
+        timer.time_calls(lambda: h.gather_gemm(X, W, gathered, out), 1)
+        st = h.read_stats()
+        spans.append((st[2] - st[1]) / 1e6)
+    h.set_option(tovl.OPT_STATS, 0)
+    t_comp_fused = statistics.median(spans)
+    overlap = (t_comp + t_comm - t_total) / min(t_comp, t_comm)
+    return {
+        "T_comp_alone_ms": t_comp, "T_comm_alone_ms": t_comm, "T_total_ms": t_total,
+        "T_comp_at_fused_ms": t_comp_fused,
+        "overlap_efficiency": overlap, "overlap_target": 0.8,
+        "compute_interference": t_comp_fused / t_comp, "interference_target": 1.1,
+        "producer_ctas": h.get_option(tovl.OPT_PRODUCERS), "consumer_ctas": h.get_option(tovl.OPT_CONSUMERS),
+    }
+
+
+def e2e_tp(h, cfg, W, gathered, out, steps: int, stream):
+    """Host shards -> device, fused call, device -> host output, per step."""
+    import torch
+    import workloads
+    X_host = workloads.gather_inputs(cfg, 0, "cpu")[0].pin_memory()
+    out_host = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16).pin_memory()
+    X_dev = torch.empty_like(X_host, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def step():
+        X_dev.copy_(X_host, non_blocking=True)
+        h.gather_gemm(X_dev, W, gathered, out, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        ev[0].record(stream)
+        for _ in range(steps):
+            step()
+        ev[1].record(stream)
+    stream.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / steps
+    return {"value": cfg.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": X_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
+
+
+def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int):
+    """Dispatch + grouped GEMM: algorithmic TFLOP/s (real rows only)."""
+    import numpy as np
+    import torch
+    import oracle  # noqa: F401  (routing counts only come from the plan below)
+    import workloads
+    from consumer_movement_gemm_gb300 import tovl
+    x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
+    rows = tovl.dispatch_rows(cfg.T, cfg.k, cfg.E)
+    with tovl.Handle(0, max_rows=rows, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=k_slices) as h:
+        if producers:
+            h.set_option(tovl.OPT_PRODUCERS, producers)
+        topk = torch.from_numpy(topk_np).to(dev)
+        dispatched = torch.zeros(rows, cfg.H, dtype=torch.bfloat16, device=dev)
+        offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+        out = torch.empty(rows, cfg.N, dtype=torch.bfloat16, device=dev)
+        stream = torch.cuda.current_stream()
+        timer = Timer(stream)
+        fn = lambda: h.dispatch_grouped_gemm(x, topk, W, dispatched, offs, out)  # noqa: E731
+        timer.time_calls(fn, 3)
+        ms = statistics.median(timer.time_calls(fn, rounds))
+        assert h.sync_status() == 0
+        counts = np.bincount(topk_np.reshape(-1), minlength=cfg.E)
+        m_pad = int(offs[-1].item())
+        flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.N
+        return {"workload": cfg.name, "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+                "algorithmic_GFLOP": flops / 1e9, "padded_rows": m_pad, "max_expert_rows": int(counts.max()),
+                "min_expert_rows": int(counts.min()), "rounds": rounds, "l2": "flushed before every round"}
+
+
+def copy_sweep(rounds: int, dev, sizes):
+    import numpy as np
+    import torch
+    import workloads
+    from consumer_movement_gemm_gb300 import tovl
+    cfg = workloads.COPY
+    n = cfg.n_rows
+    perm = torch.from_numpy(workloads.permutation(n, cfg.seed)).to(dev)
+    res = []
+    big = max(sizes)
+    src_all = torch.empty(n * big, dtype=torch.uint8, device=dev)
+    dst_all = torch.empty(n * big, dtype=torch.uint8, device=dev)
+    src_all.random_(0, 256)
+    with tovl.Handle(0, max_rows=n) as h:
+        stream = torch.cuda.current_stream()
+        timer = Timer(stream)
+        for rb in sizes:
+            src = src_all[: n * rb].view(n, rb)
+            dst = dst_all[: n * rb].view(n, rb)
+            for mode in (tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK):
+                h.set_option(tovl.OPT_COPY_MODE, mode)
+                row = {"row_bytes": rb, "copy_mode": "vector" if mode == 0 else "bulk"}
+                for gated in (False, True):
+                    fn = lambda: h.gated_copy(src, dst, perm, gated=gated)  # noqa: E731
+                    timer.time_calls(fn, 2, flush=False)
+                    ms = statistics.median(timer.time_calls(fn, rounds, flush=False))
+                    row["gated_GBps" if gated else "ungated_GBps"] = 2.0 * n * rb / (ms * 1e-3) / 1e9
+                h.gated_copy(src, dst, perm, gated=True, stamps=True)
+                assert h.sync_status() == 0
+                pub, obs = h.read_latency((n + 63) // 64)
+                lat = (obs - pub).astype(np.float64) / 1e3
+                row["signal_wait_us_median"] = float(np.median(lat))
+                row["signal_wait_us_p99"] = float(np.percentile(lat, 99))
+                res.append(row)
+    return {"workload": cfg.name, "rows": n, "rounds": rounds,
+            "l2": "inputs larger than L2 (no flush)", "sweep": res}
+
+
+def run_tovl(args):
+    import torch
+    import workloads
+    from consumer_movement_gemm_gb300 import build as tovl_build
+    from consumer_movement_gemm_gb300 import tovl
+
+    rank, world, local = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = "cuda"
+    if rank == 0 or world > 1:
+        tovl_build.build()
+    barrier(world)
+    cfg = workloads.TP
+    peaks, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    h = tovl.Handle(local, max_rows=1 << 14, producer_ctas=args.producers, k_slices=args.k_slices)
+    X, W, gathered, out = tp_setup(h, cfg, dev)
+    timer = Timer(stream)
+    step = lambda: h.gather_gemm(X, W, gathered, out, stream=stream)  # noqa: E731
+    timer.time_calls(step, args.warmup)
+    assert h.sync_status() == 0
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        times = timer.time_calls(step, args.steps)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    assert h.sync_status() == 0
+    ms = statistics.mean(times)
+    ms_max = max_over_ranks(ms, world)
+    value = sum_over_ranks(cfg.flops, world) / (ms_max * 1e-3) / 1e12
+
+    acc = acceptance(h, timer, cfg, X, W, gathered, out, 50)
+    e2e = e2e_tp(h, cfg, W, gathered, out, 50, stream)
+
+    extra = {}
+    if args.sweep:
+        sweep = []
+        for P in [4, 8, 16, 24, 32]:
+            h.set_option(tovl.OPT_PRODUCERS, P)
+            a = acceptance(h, timer, cfg, X, W, gathered, out, 30)
+            a["TFLOP/s"] = cfg.flops / (a["T_total_ms"] * 1e-3) / 1e12
+            sweep.append(a)
+        h.set_option(tovl.OPT_PRODUCERS, acc["producer_ctas"])
+        extra["producer_sweep"] = sweep
+        ks = []
+        for S in [1, 2, 4, 8]:
+            with tovl.Handle(local, max_rows=1 << 14, producer_ctas=acc["producer_ctas"], k_slices=S) as hs:
+                a = acceptance(hs, timer, cfg, X, W, gathered, out, 30)
+                a["k_slices"] = S
+                a["TFLOP/s"] = cfg.flops / (a["T_total_ms"] * 1e-3) / 1e12
+                ks.append(a)
+        extra["k_slices_sweep"] = ks
+    h.close()
+    if not args.quick:
+        extra["dispatch_uniform"] = dispatch_bench(workloads.DISPATCH, 30 if not args.full else workloads.DISPATCH.rounds * 10,
+                                                   dev, args.producers, args.k_slices)
+        extra["dispatch_zipf"] = dispatch_bench(workloads.SKEWED, 20 if not args.full else workloads.SKEWED.rounds * 10,
+                                                dev, args.producers, args.k_slices)
+        sizes = list(workloads.COPY.row_sizes)
+        extra["gated_copy"] = copy_sweep(1000 if args.full else 20, dev, sizes)
+
+    if rank != 0:
+        return
+    tf = cfg.flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = recorded_traffic("fused_gather_gemm_tp.md", "consumer_movement_gemm_gb300/csrc/fused.cu")
+    cpu = cpu_oracle_sample(cfg, args.cpu_seconds)
+    cpu.pop("seconds", None)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "shards": cfg.shards, "rows_per_shard": cfg.rows_per_shard, "K": cfg.K,
+                   "N": cfg.N, "parallelism": "replicas only" if world > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "producer_ctas": acc["producer_ctas"], "consumer_ctas": acc["consumer_ctas"],
+                   "k_slices": args.k_slices},
+        "overlap_efficiency": acc["overlap_efficiency"],
+        "gated_copy_GBps": (max(r["gated_GBps"] for r in extra["gated_copy"]["sweep"])
+                            if "gated_copy" in extra else None),
+        "acceptance": acc,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
+                     "frac_of_sustained": tf / peaks.get("bf16_tflops_sustained", peak)},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": t_wall,
+        "configs": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_tovl(args)
+
+
+if __name__ == "__main__":
+    main()

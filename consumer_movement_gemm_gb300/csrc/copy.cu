@@ -26,11 +26,21 @@ constexpr int kCopySmem = 200 * 1024;
 __device__ __forceinline__ void chunk_arrive(const CopyParams& p, long long dst_row)
 {
     const int c = static_cast<int>(dst_row / kChunkRows);
-    const int old = ptx::atom_add_acq_rel_gpu(p.ctrl.cnt + c, 1);
+    const int cs = c * p.ctrl.n_slices;            // a copy is not sliced: slice 0 carries the rows
+    const int old = ptx::atom_add_acq_rel_gpu(p.ctrl.cnt + cs, 1);
     if (old + 1 == p.seq * kChunkRows) {
         if (p.stamps) p.ctrl.pub_ns[c] = static_cast<long long>(ptx::globaltimer());
-        ptx::st_release_gpu(p.ctrl.slot + c, p.seq);
+        ptx::st_release_gpu(p.ctrl.slot + cs, p.seq);
     }
+}
+
+// The elected arrival of chunk c (its relaxed add completed the count):
+// acquire every earlier arrival, then publish the round's sequence.
+__device__ __forceinline__ void publish_chunk(const CopyParams& p, int c)
+{
+    ptx::fence_acq_rel_gpu();
+    if (p.stamps) p.ctrl.pub_ns[c] = static_cast<long long>(ptx::globaltimer());
+    ptx::st_release_gpu(p.ctrl.slot + c * p.ctrl.n_slices, p.seq);
 }
 
 // Counters this copy does not fill to their per-round quota get the missing
@@ -38,16 +48,17 @@ __device__ __forceinline__ void chunk_arrive(const CopyParams& p, long long dst_
 // row-block counter).
 __device__ void copy_seeds(const CopyParams& p, int tid, int n_threads)
 {
-    for (int c = tid; c < p.ctrl.n_chunk_cap; c += n_threads) {
-        const long long real = min(max(p.n_rows - static_cast<long long>(c) * kChunkRows, 0LL),
-                                   static_cast<long long>(kChunkRows));
+    const int S = p.ctrl.n_slices;
+    for (int cs = tid; cs < p.ctrl.n_chunk_cap * S; cs += n_threads) {
+        const int c = cs / S;
+        const long long real = (cs % S) ? 0LL
+                                        : min(max(p.n_rows - static_cast<long long>(c) * kChunkRows, 0LL),
+                                              static_cast<long long>(kChunkRows));
         const int seed = kChunkRows - static_cast<int>(real);
-        if (seed > 0) {
-            const int old = ptx::atom_add_acq_rel_gpu(p.ctrl.cnt + c, seed);
-            if (old + seed == p.seq * kChunkRows) ptx::st_release_gpu(p.ctrl.slot + c, p.seq);
-        }
+        if (seed > 0) arrive_and_publish(p.ctrl, cs, seed, p.seq);
     }
-    for (int b = tid; b < p.ctrl.n_block_cap; b += n_threads) ptx::red_add_release_gpu(p.ctrl.rbcnt + b, kBlockRows);
+    for (int bs = tid; bs < p.ctrl.n_block_cap * S; bs += n_threads)
+        ptx::red_add_release_gpu(p.ctrl.rbcnt + bs, kBlockRows);
 }
 
 // Vector copy: each warp takes a group of consecutive source rows (about
@@ -57,7 +68,7 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
 {
     const uint32_t lane = ptx::lane_id();
     const int n16 = p.row_bytes / 16;
-    const int rows_per_group = max(1, 16384 / p.row_bytes);
+    const int rows_per_group = min(64, max(1, 16384 / p.row_bytes));   // at most two rows per lane
     const long long n_groups = (p.n_rows + rows_per_group - 1) / rows_per_group;
     for (long long g = gw; g < n_groups; g += n_gw) {
         const long long r0 = g * rows_per_group;
@@ -84,8 +95,25 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
             }
         }
         if (p.gated) {
+            // One release fence covers the warp's row stores (ordered before
+            // it by the warp barrier); the arrivals are then relaxed atomics,
+            // so a lane's two arrivals are in flight together.  A lane whose
+            // arrival completes a chunk takes an acquire fence before
+            // publishing -- together the acq_rel counting of section 3.
             __syncwarp();
-            for (int rr = lane; rr < nr; rr += 32) chunk_arrive(p, p.perm[r0 + rr]);
+            ptx::fence_acq_rel_gpu();
+            const int S = p.ctrl.n_slices;
+            int c0 = -1, c1 = -1, o0 = 0, o1 = 0;
+            if (static_cast<int>(lane) < nr) {
+                c0 = p.perm[r0 + lane] / kChunkRows;
+                o0 = ptx::atom_add_relaxed_gpu(p.ctrl.cnt + c0 * S, 1);
+            }
+            if (static_cast<int>(lane) + 32 < nr) {
+                c1 = p.perm[r0 + lane + 32] / kChunkRows;
+                o1 = ptx::atom_add_relaxed_gpu(p.ctrl.cnt + c1 * S, 1);
+            }
+            if (c0 >= 0 && o0 + 1 == p.seq * kChunkRows) publish_chunk(p, c0);
+            if (c1 >= 0 && o1 + 1 == p.seq * kChunkRows) publish_chunk(p, c1);
         }
     }
 }
@@ -132,7 +160,7 @@ __device__ void copy_waiter(const CopyParams& p, int ww, int n_ww)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int c = c0 + static_cast<int>(lane) + 32 * (j + u);
-                val[u] = (j + u < cpl && c < c1 && !((seen_bits >> (j + u)) & 1ull)) ? ptx::ld_acquire_gpu(p.ctrl.slot + c)
+                val[u] = (j + u < cpl && c < c1 && !((seen_bits >> (j + u)) & 1ull)) ? ptx::ld_acquire_gpu(p.ctrl.slot + c * p.ctrl.n_slices)
                                                                                         : -2147483647;
             }
 #pragma unroll

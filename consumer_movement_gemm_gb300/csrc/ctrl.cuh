@@ -19,7 +19,12 @@ constexpr int kTileN = 256;
 constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 192;      // 6 warps: TMA, MMA, 4 x epilogue (consumers) / copy warps (producers)
+constexpr int kThreads = 384;      // 12 warps: TMA, MMA, 8 x epilogue, 2 idle (consumers) / 12 copy warps (producers)
+constexpr int kEpiWarp0 = 2;       // first epilogue warp
+constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each owning 128 of the 256 columns
+constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
+constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)
+constexpr int kReleaseBatch = 4;   // producer items per batched release
 constexpr int kMaxShards = 64;
 constexpr int kMaxExperts = 512;
 
@@ -62,6 +67,7 @@ struct Ctrl {
     long long* obs_ns;    // [n_chunk_cap]  first observation time by a waiter
     int n_chunk_cap;
     int n_block_cap;
+    int n_slices;         // K-slices per chunk / block; slot, cnt and rbcnt hold n_slices entries per chunk / block
 };
 
 // Routing plan produced on the device for one dispatch round.
@@ -95,9 +101,11 @@ struct FusedParams {
     int gate_seq;         // sequence the consumer gates wait for (seq, unless a fault is injected)
     long long timeout_ns; // bound of a gate wait on other CTAs
     long long pipe_timeout_ns;  // bound of a wait on this CTA's own pipeline (outlasts a gate timeout)
-    int copy_mode;        // 0: 16-byte vector copies, 1: bulk async copies through shared memory
     int stats;
     int row_bytes;        // K * 2
+    int k_slices;         // K-slices in use this call (<= ctrl.n_slices); slices beyond are seeded
+    int wave_blocks;      // row blocks the consumers' first wave covers (producer ordering group)
+    int item_rows;        // rows per producer item (a power of two dividing 64)
     // gather sources
     const void* shard[kMaxShards];
     int n_shards;

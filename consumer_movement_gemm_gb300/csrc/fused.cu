@@ -2,23 +2,31 @@
 //
 // One cooperative launch of P producer CTAs and C consumer CTAs, one CTA per
 // SM, all co-resident:
-//   producers  copy token rows into the gathered (or dispatched) buffer and
-//              count them with the single-writer protocol: 64-row chunk
-//              watermarks published by an elected last arrival (gather), or
-//              release reductions into 128-row block counters pre-seeded
-//              with the padding count (dispatch)  -- "cross-GPU sync
+//   producers  copy token rows into the gathered (or dispatched) buffer with
+//              16-byte vector loads/stores and count them with the
+//              single-writer protocol: an acq_rel arrival count per 64-row
+//              chunk whose last arrival is elected to release-store the
+//              round's sequence number into the chunk's watermark slot
+//              (gather), or release reductions into 128-row block counters
+//              pre-seeded with the padding count (dispatch) -- "cross-GPU sync
 //              protocols on PCIe", sections 3-5;
 //   consumers  run a tcgen05 bf16 GEMM over 128x256 output tiles in
-//              row-block order (the producers' order, section 6 item 3); the
-//              TMA warp of each consumer gates every new row block on the
-//              protocol with acquire polls before loading it.
+//              row-block order; the TMA warp of each consumer gates the rows
+//              of a tile on the protocol with acquire polls before loading
+//              them.
+// Each chunk watermark may be split along K into k_slices sub-watermarks:
+// the consumer's minimal release unit is a K-range of a row block, and the
+// signal follows it (section 4: signal granularity follows the consumer's
+// release unit).  Producers copy in the consumers' traversal order -- first
+// wave's row blocks, slice by slice, then the next wave's (section 6, item 3)
+// -- so the first tiles start after a fraction of their rows has landed.
+// With k_slices = 1 each slot is exactly one 64-row chunk watermark.
 // Producers never wait on anyone; consumers wait only on producers, which are
 // resident by construction (cooperative launch), and every wait is bounded.
 #include <cuda_runtime.h>
 #include "ctrl.cuh"
 #include "ptx.cuh"
 #include "sync.cuh"
-#include "copyplane.cuh"
 #include "launch.cuh"
 
 namespace tovl {
@@ -43,18 +51,17 @@ __device__ __forceinline__ void stat_max(const FusedParams& p, int idx, unsigned
     if (p.stats) atomicMax(p.ctrl.stats + idx, v);
 }
 
-// Number of 128-row blocks the consumers traverse.
+// Number of 128-row blocks the consumers traverse this round.
 __device__ __forceinline__ int num_row_blocks(const FusedParams& p)
 {
     if (p.mode == kModeGather) return (p.M + kTileM - 1) / kTileM;
     return p.meta[1];
 }
 
-// Rows of the gathered/dispatched buffer the producers fill this round.
-__device__ __forceinline__ int num_rows(const FusedParams& p)
+// K-blocks [kb_begin(s), kb_begin(s+1)) form slice s.
+__device__ __forceinline__ int kb_begin(const FusedParams& p, int s)
 {
-    if (p.mode == kModeGather) return p.M;
-    return p.meta[0];
+    return s * p.n_kb / p.k_slices;
 }
 
 // ============================================================= consumers
@@ -82,64 +89,70 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t* smem)
     return s;
 }
 
-// TMA warp: gate each new row block, then stream A and B k-blocks.
+// Gate: the rows of row block mb, K-slice s, are complete this round.
+__device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb, int s)
+{
+    const int* words[kTileM / kChunkRows];
+    int n = 0;
+    int target;
+    const int S = p.ctrl.n_slices;
+    if (p.mode == kModeGather) {
+        const int c0 = mb * (kTileM / kChunkRows);
+        for (int i = 0; i < kTileM / kChunkRows; ++i)
+            if ((c0 + i) * kChunkRows < p.M) words[n++] = p.ctrl.slot + (c0 + i) * S + s;
+        target = p.gate_seq;
+    } else {
+        words[n++] = p.ctrl.rbcnt + mb * S + s;
+        target = p.gate_seq * kBlockRows;
+    }
+    const int r = warp_wait_ge(words, n, target, p.ctrl, p.seq, p.timeout_ns);
+    // the rows were written through the generic proxy; order them before
+    // this thread's tensor-memory-access (async proxy) reads
+    if (ptx::lane_id() == 0) ptx::fence_proxy_async_global();
+    return static_cast<unsigned long long>(r < 0 ? -r : r);
+}
+
+// TMA warp: per tile and K-slice, gate the slice's rows, then stream A and B
+// k-blocks into the stage ring.
 __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles)
 {
     const uint32_t lane = ptx::lane_id();
     uint32_t stage = 0, phase = 0;
-    int gated_mb = -1;
     unsigned long long polls = 0;
-    for (int t = cid; t < n_tiles; t += p.n_consumers) {
+    int fail = 0;
+    for (int t = cid; t < n_tiles && !fail; t += p.n_consumers) {
         const int mb = t / p.n_nb;
         const int nb = t % p.n_nb;
-        int brow = 0;
-        if (p.mode == kModeDispatch) brow = p.blk_expert[mb] * p.K;
-        if (p.gated && mb != gated_mb) {
-            const int* words[2];
-            int n = 0;
-            int target;
-            if (p.mode == kModeGather) {
-                const int c0 = mb * (kTileM / kChunkRows);
-                for (int i = 0; i < kTileM / kChunkRows; ++i)
-                    if ((c0 + i) * kChunkRows < p.M) words[n++] = p.ctrl.slot + c0 + i;
-                target = p.gate_seq;
-            } else {
-                words[n++] = p.ctrl.rbcnt + mb;
-                target = p.gate_seq * kBlockRows;
-            }
-            const int r = warp_wait_ge(words, n, target, p.ctrl, p.seq, p.timeout_ns);
-            polls += static_cast<unsigned long long>(r < 0 ? -r : r);
-            gated_mb = mb;
-            // the gathered rows were written through the generic proxy (or
-            // bulk copies); order them before this thread's TMA reads.
-            if (lane == 0) ptx::fence_proxy_async_global();
-        }
-        int fail = 0;
-        if (lane == 0) {
-            for (int kb = 0; kb < p.n_kb; ++kb) {
-                if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) {
-                    fail = 1;
-                    break;
-                }
-                ptx::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-                ptx::tma_load_2d(s.a + stage * kStageA, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
-                uint8_t* bdst = s.b + stage * kStageB;
+        const int brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
+        for (int sl = 0; sl < p.k_slices && !fail; ++sl) {
+            if (p.gated) polls += gate(p, mb, sl);
+            if (lane == 0) {
+                const int kb1 = kb_begin(p, sl + 1);
+                for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) {
+                        fail = 1;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
+                    ptx::tma_load_2d(s.a + stage * kStageA, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
+                    uint8_t* bdst = s.b + stage * kStageB;
 #pragma unroll
-                for (int j = 0; j < kTileN / 64; ++j)
-                    ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[stage], nb * kTileN + j * 64,
-                                     brow + kb * kTileK);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                    for (int j = 0; j < kTileN / 64; ++j)
+                        ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[stage], nb * kTileN + j * 64,
+                                         brow + kb * kTileK);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
+            fail = __shfl_sync(0xffffffffu, fail, 0);
         }
-        if (__shfl_sync(0xffffffffu, fail, 0)) break;
     }
     if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
 }
 
-// MMA warp: one elected lane issues tcgen05.mma into a double-buffered TMEM
+// MMA warp: one lane issues tcgen05.mma into a double-buffered TMEM
 // accumulator (2 x 256 fp32 columns).
 __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles, uint32_t tmem_base)
 {
@@ -178,12 +191,15 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem& s, int ci
 }
 
 // Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) -> out.
+// Warp w reads TMEM lane quarter w % 4 (the quarter its position allows) and
+// one half of the 256 accumulator columns.
 __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles,
                                   uint32_t tmem_base, int valid_rows)
 {
     const int warp = threadIdx.x / 32;
     const uint32_t lane = ptx::lane_id();
-    const int q = warp & 3;                       // TMEM lane quarter this warp may access
+    const int q = warp & 3;
+    const int half = (warp - kEpiWarp0) / 4;
     const int row_in_tile = q * 32 + static_cast<int>(lane);
     uint16_t* out = static_cast<uint16_t*>(p.out);
     int local = 0;
@@ -197,10 +213,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem& s, i
         ptx::tc_fence_after();
         const int row = mb * kTileM + row_in_tile;
         const bool ok = row < valid_rows;
-        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + nb * kTileN);
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
+        const int col0 = half * (kTileN / 2);
+        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + nb * kTileN + col0);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + col0;
 #pragma unroll 1
-        for (int c = 0; c < kTileN / 32; ++c) {
+        for (int c = 0; c < kTileN / 2 / 32; ++c) {
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
             ptx::tmem_ld_wait();
@@ -232,7 +249,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&s.tfull[i], 1);
-            ptx::mbar_init(&s.tempty[i], 4 * 32);
+            ptx::mbar_init(&s.tempty[i], kEpiWarps * 32);
         }
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
@@ -252,7 +269,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     const int valid_rows = (p.mode == kModeGather) ? p.M : p.meta[0];
     if (warp == 0) consumer_tma(p, s, cid, n_tiles);
     else if (warp == 1) consumer_mma(p, s, cid, n_tiles, tmem_base);
-    else consumer_epilogue(p, s, cid, n_tiles, tmem_base, valid_rows);
+    else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue(p, s, cid, n_tiles, tmem_base, valid_rows);
     __syncwarp();
 
     // teardown: full-CTA barrier 0, after every role has finished
@@ -266,146 +283,185 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 }
 
 // ============================================================= producers
-// Completion of one copied row.
-__device__ __forceinline__ void row_done(const FusedParams& p, int r)
+// Row-block-slice items: item i -> (row block mb, K-slice s, row group q)
+// in the consumers' order: groups of wave_blocks row blocks, each group slice
+// by slice, each slice block by block.
+struct Item {
+    int mb, s, r0;
+};
+
+__device__ __forceinline__ Item decode_item(const FusedParams& p, int i, int n_blocks)
 {
-    if (p.mode == kModeGather) {
-        arrive_and_publish(p.ctrl, r / kChunkRows, 1, p.seq);
-    } else {
-        ptx::red_add_release_gpu(p.ctrl.rbcnt + r / kBlockRows, 1);
-    }
+    const int ipb = kBlockRows / p.item_rows;              // items per block per slice
+    const int per_group = p.wave_blocks * p.k_slices * ipb;
+    const int g = i / per_group;
+    const int b0 = g * p.wave_blocks;
+    const int gs = min(p.wave_blocks, n_blocks - b0);
+    const int rem = i - g * per_group;
+    Item it;
+    it.s = rem / (gs * ipb);
+    const int rem2 = rem - it.s * gs * ipb;
+    it.mb = b0 + rem2 / ipb;
+    it.r0 = it.mb * kBlockRows + (rem2 % ipb) * p.item_rows;
+    return it;
 }
 
+// Source address of destination row r (nullptr: no source, padding row).
 __device__ __forceinline__ const uint8_t* row_src(const FusedParams& p, int r)
 {
     if (p.mode == kModeGather) {
+        if (r >= p.M) return nullptr;
         const int s = r / p.rows_per_shard;
         const int i = r - s * p.rows_per_shard;
         return static_cast<const uint8_t*>(p.shard[s]) + static_cast<size_t>(i) * p.row_bytes;
     }
-    return static_cast<const uint8_t*>(p.x) + static_cast<size_t>(p.src_of_dst[r]) * p.row_bytes;
+    const int t = p.src_of_dst[r];
+    return t < 0 ? nullptr : static_cast<const uint8_t*>(p.x) + static_cast<size_t>(t) * p.row_bytes;
 }
 
-__device__ __forceinline__ bool row_real(const FusedParams& p, int r)
+// Counter index and completion of an item's rows.
+__device__ __forceinline__ void item_done(const FusedParams& p, int counter, int n)
 {
-    return p.mode == kModeGather || p.src_of_dst[r] >= 0;
+    if (p.mode == kModeGather) arrive_and_publish(p.ctrl, counter, n, p.seq);
+    else ptx::red_add_release_gpu(p.ctrl.rbcnt + counter, n);
 }
 
 // Per-round padding seeds.  Each counter must gain exactly its per-round
-// quota (64 per chunk, 128 per row block) every call, so counters this call
-// does not fill receive the missing arrivals as one seed add.
+// quota (64 per chunk slice, 128 per block slice) every call, so whatever
+// this call does not fill -- rows past the end, padding rows, slices beyond
+// k_slices, blocks beyond this round -- is added as one seed.
 __device__ void seed_counters(const FusedParams& p, int gw, int n_gw)
 {
     const uint32_t lane = ptx::lane_id();
     const Ctrl& c = p.ctrl;
-    // chunk counters
-    for (int ch = gw * 32 + lane; ch < c.n_chunk_cap; ch += n_gw * 32) {
+    const int S = c.n_slices;
+    // chunk-slice counters
+    for (int cs = gw * 32 + lane; cs < c.n_chunk_cap * S; cs += n_gw * 32) {
+        const int ch = cs / S, sl = cs - ch * S;
         int seed = kChunkRows;
-        if (p.mode == kModeGather) {
-            const int real = min(max(p.M - ch * kChunkRows, 0), kChunkRows);
-            seed = kChunkRows - real;
-        }
-        if (seed > 0) arrive_and_publish(c, ch, seed, p.seq);
+        if (p.mode == kModeGather && sl < p.k_slices) seed = kChunkRows - min(max(p.M - ch * kChunkRows, 0), kChunkRows);
+        if (seed > 0) arrive_and_publish(c, cs, seed, p.seq);
     }
-    // row-block counters
+    // block-slice counters
     if (p.mode == kModeGather) {
-        for (int b = gw * 32 + lane; b < c.n_block_cap; b += n_gw * 32) ptx::red_add_release_gpu(c.rbcnt + b, kBlockRows);
+        for (int bs = gw * 32 + lane; bs < c.n_block_cap * S; bs += n_gw * 32)
+            ptx::red_add_release_gpu(c.rbcnt + bs, kBlockRows);
         return;
     }
     const int n_blocks = p.meta[1];
     const int zero = p.meta[2];
     for (int b = gw; b < c.n_block_cap; b += n_gw) {
         if (b >= n_blocks) {
-            if (lane == 0) ptx::red_add_release_gpu(c.rbcnt + b, kBlockRows);
+            if (static_cast<int>(lane) < S) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, kBlockRows);
             continue;
         }
         const int pad = p.pad[b];
-        if (pad == 0) continue;
-        if (zero) {
+        if (zero && pad > 0) {
             // padding rows are the last `pad` rows of the block; they must be
-            // zero before the counter reaches its target
-            uint8_t* base = static_cast<uint8_t*>(p.gathered) +
-                            static_cast<size_t>(b * kBlockRows + kBlockRows - pad) * p.row_bytes;
-            int4* d = reinterpret_cast<int4*>(base);
+            // zero before the counters reach their target
+            int4* d = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.gathered) +
+                                              static_cast<size_t>(b * kBlockRows + kBlockRows - pad) * p.row_bytes);
             const size_t n16 = static_cast<size_t>(pad) * p.row_bytes / 16;
             const int4 z = make_int4(0, 0, 0, 0);
             for (size_t i = lane; i < n16; i += 32) ptx::st_v4(d + i, z);
             __syncwarp();
         }
-        if (lane == 0) ptx::red_add_release_gpu(c.rbcnt + b, pad);
+        // slices beyond k_slices get the whole block quota, the others the padding count
+        if (static_cast<int>(lane) < S) {
+            const int seed = static_cast<int>(lane) < p.k_slices ? pad : kBlockRows;
+            if (seed > 0) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, seed);
+        }
     }
 }
 
-// 16-byte vector copy, one warp per row.
-__device__ void producer_v4(const FusedParams& p, int gw, int n_gw)
+// Copy one item: item_rows destination rows x the K-slice's bytes, as one
+// flat range of 16-byte words, up to 16 per lane in flight.
+__device__ __forceinline__ int copy_item(const FusedParams& p, const Item& it, const uint8_t** tbl)
 {
     const uint32_t lane = ptx::lane_id();
-    const int rows = num_rows(p);
-    const int n16 = p.row_bytes / 16;
-    for (int r = gw; r < rows; r += n_gw) {
-        if (!row_real(p, r)) continue;
-        const int4* s = reinterpret_cast<const int4*>(row_src(p, r));
-        int4* d = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.gathered) + static_cast<size_t>(r) * p.row_bytes);
-        int i = lane;
-        for (; i + 96 < n16; i += 128) {
-            const int4 v0 = ptx::ld_nc_v4(s + i);
-            const int4 v1 = ptx::ld_nc_v4(s + i + 32);
-            const int4 v2 = ptx::ld_nc_v4(s + i + 64);
-            const int4 v3 = ptx::ld_nc_v4(s + i + 96);
-            ptx::st_v4(d + i, v0);
-            ptx::st_v4(d + i + 32, v1);
-            ptx::st_v4(d + i + 64, v2);
-            ptx::st_v4(d + i + 96, v3);
+    const int RI = p.item_rows;
+    for (int l = lane; l < RI; l += 32) tbl[l] = row_src(p, it.r0 + l);
+    __syncwarp();
+    const size_t soff = static_cast<size_t>(kb_begin(p, it.s)) * kTileK * 2;
+    const int n16 = (kb_begin(p, it.s + 1) - kb_begin(p, it.s)) * kTileK * 2 / 16;
+    uint8_t* dst = static_cast<uint8_t*>(p.gathered) + soff + static_cast<size_t>(it.r0) * p.row_bytes;
+    // lane position (row, col) in the item's flat range of 16-byte words,
+    // advanced by 32 words per step without division
+    int row = static_cast<int>(lane) / n16;
+    int col = static_cast<int>(lane) - row * n16;
+    while (row < RI) {
+        int4 v[kItemInt4 / 32];
+        int r = row, c = col;
+#pragma unroll
+        for (int j = 0; j < kItemInt4 / 32; ++j) {
+            if (r < RI) {
+                const uint8_t* src = tbl[r];
+                if (src) v[j] = ptx::ld_nc_v4(reinterpret_cast<const int4*>(src + soff) + c);
+            }
+            c += 32;
+            while (c >= n16) {
+                c -= n16;
+                ++r;
+            }
         }
-        for (; i < n16; i += 32) ptx::st_v4(d + i, ptx::ld_nc_v4(s + i));
-        __syncwarp();
-        if (lane == 0) row_done(p, r);
+        r = row;
+        c = col;
+#pragma unroll
+        for (int j = 0; j < kItemInt4 / 32; ++j) {
+            if (r < RI && tbl[r]) ptx::st_v4(reinterpret_cast<int4*>(dst + static_cast<size_t>(r) * p.row_bytes) + c, v[j]);
+            c += 32;
+            while (c >= n16) {
+                c -= n16;
+                ++r;
+            }
+        }
+        row = r;
+        col = c;
     }
+    // rows this item filled
+    int n = 0;
+    for (int l = 0; l < RI; l += 32) {
+        const bool real = (l + static_cast<int>(lane) < RI) && tbl[l + lane] != nullptr;
+        n += __popc(__ballot_sync(0xffffffffu, real));
+    }
+    __syncwarp();
+    return n;
 }
-
-// Rows this issuer moves with bulk copies: rows g, g + n_g, ... (real rows only).
-struct FusedRowJob {
-    const FusedParams* p;
-    int cursor;
-    int step;
-    int rows;
-    __device__ int next()
-    {
-        while (cursor < rows) {
-            const int r = cursor;
-            cursor += step;
-            if (row_real(*p, r)) return r;
-        }
-        return -1;
-    }
-    __device__ const void* src(int r) { return row_src(*p, r); }
-    __device__ void* dst(int r)
-    {
-        return static_cast<uint8_t*>(p->gathered) + static_cast<size_t>(r) * p->row_bytes;
-    }
-    __device__ void done(int r) { row_done(*p, r); }
-};
 
 __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
 {
     const int warp = threadIdx.x / 32;
+    const uint32_t lane = ptx::lane_id();
     const int n_warps = kThreads / 32;
+    const int gw = pid * n_warps + warp;
+    const int n_gw = p.n_producers * n_warps;
     if (threadIdx.x == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
-    if (p.copy_mode == 0) {
-        seed_counters(p, pid * n_warps + warp, p.n_producers * n_warps);
-        producer_v4(p, pid * n_warps + warp, p.n_producers * n_warps);
-    } else {
-        if (warp == 0) {
-            if (ptx::lane_id() == 0) {
-                FusedRowJob job{&p, pid, p.n_producers, num_rows(p)};
-                const Ring ring = make_ring(smem, kStages * kStageBytes, p.row_bytes);
-                run_bulk(job, static_cast<uint32_t>(p.row_bytes), ring, p.ctrl, p.pipe_timeout_ns);
-            }
+    seed_counters(p, gw, n_gw);
+
+    const uint8_t** tbl = reinterpret_cast<const uint8_t**>(smem) + warp * 64;   // row-source table per warp
+    const int n_blocks = num_row_blocks(p);
+    const int n_items = n_blocks * p.k_slices * (kBlockRows / p.item_rows);
+    const int S = p.ctrl.n_slices;
+    // lane j < kReleaseBatch holds the j-th pending item of the batch
+    int pend_counter = 0, pend_n = 0, n_pend = 0;
+    for (int i = gw; i < n_items; i += n_gw) {
+        const Item it = decode_item(p, i, n_blocks);
+        const int n = copy_item(p, it, tbl);
+        const int counter = (p.mode == kModeGather) ? (it.r0 / kChunkRows) * S + it.s : it.mb * S + it.s;
+        if (static_cast<int>(lane) == n_pend) {
+            pend_counter = counter;
+            pend_n = n;
+        }
+        if (++n_pend == kReleaseBatch) {
+            // the copies above happen-before every lane's release below
             __syncwarp();
-        } else {
-            seed_counters(p, pid * (n_warps - 1) + warp - 1, p.n_producers * (n_warps - 1));
+            if (static_cast<int>(lane) < n_pend && pend_n > 0) item_done(p, pend_counter, pend_n);
+            n_pend = 0;
         }
     }
+    __syncwarp();
+    if (static_cast<int>(lane) < n_pend && pend_n > 0) item_done(p, pend_counter, pend_n);
+    __syncwarp();
     __syncthreads();
     if (threadIdx.x == 0) stat_max(p, kStatProdEndNs, ptx::globaltimer());
 }
@@ -418,10 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     if (static_cast<int>(blockIdx.x) < p.n_producers) producer(p, smem, blockIdx.x);
     else consumer(p, smem, blockIdx.x - p.n_producers);
 }
-
-}  // namespace tovl
-
-namespace tovl {
 
 cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative)
 {

@@ -69,6 +69,13 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v)
     return old;
 }
 
+__device__ __forceinline__ int atom_add_relaxed_gpu(int* p, int v)
+{
+    int old;
+    asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void red_add_release_gpu(int* p, int v)
 {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -27,7 +27,8 @@ struct tovl_ctx {
     tovl_config cfg;
     int device = 0;
     int num_sms = 0;
-    int producers = 16;
+    int producers = 0;       // 0 = automatic split per call
+    int last_P = 0, last_C = 0;
     int consumers = 0;
     int copy_mode = 1;
     int stats = 0;
@@ -35,6 +36,7 @@ struct tovl_ctx {
     int copy_ctas = 0;       // copy sweep copiers (0 = auto)
     int copy_waiters = 0;    // copy sweep waiters (0 = auto)
     int fault_gate_offset = 0;  // test hook: gates wait for seq + offset
+    int slices = 1;          // K-slices per chunk watermark (fixed per handle)
     long long seq = 0;
     Ctrl ctrl{};
     Plan plan{};
@@ -78,6 +80,7 @@ TOVL_API void tovl_default_config(tovl_config* cfg, int device)
     cfg->max_rows = 1 << 16;
     cfg->max_pairs = 1 << 16;
     cfg->max_experts = 64;
+    cfg->k_slices = 1;
 }
 
 TOVL_API const char* tovl_error_string(int code)
@@ -126,11 +129,11 @@ struct Carve {
     }
 };
 
-static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks)
+static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks, int S)
 {
-    ctrl.slot = c.take<int>(n_chunks);
-    ctrl.cnt = c.take<int>(n_chunks);
-    ctrl.rbcnt = c.take<int>(n_blocks);
+    ctrl.slot = c.take<int>(static_cast<size_t>(n_chunks) * S);
+    ctrl.cnt = c.take<int>(static_cast<size_t>(n_chunks) * S);
+    ctrl.rbcnt = c.take<int>(static_cast<size_t>(n_blocks) * S);
     ctrl.status = c.take<int>(1);
     ctrl.abort_seq = c.take<int>(1);
     ctrl.stats = c.take<unsigned long long>(kNumStats);
@@ -138,6 +141,7 @@ static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks)
     ctrl.obs_ns = c.take<long long>(n_chunks);
     ctrl.n_chunk_cap = n_chunks;
     ctrl.n_block_cap = n_blocks;
+    ctrl.n_slices = S;
 }
 
 static void carve_plan(Carve& c, Plan& p, int E, int max_seg, int max_pairs, long long rows, int n_blocks)
@@ -168,6 +172,8 @@ TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
     if (cfg.max_experts < 0 || cfg.max_experts > kMaxExperts) return TOVL_ERR_INVALID;
     if (cfg.producer_ctas < 0 || cfg.consumer_ctas < 0 || cfg.wait_timeout_ns < 0) return TOVL_ERR_INVALID;
     if (cfg.copy_mode != TOVL_COPY_VECTOR && cfg.copy_mode != TOVL_COPY_BULK) return TOVL_ERR_INVALID;
+    if (cfg.k_slices == 0) cfg.k_slices = 1;
+    if (cfg.k_slices < 1 || cfg.k_slices > kMaxSlices) return TOVL_ERR_INVALID;
 
     int n_dev = 0;
     if (cudaGetDeviceCount(&n_dev) != cudaSuccess || n_dev == 0) {
@@ -184,9 +190,10 @@ TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
     h->cfg = cfg;
     h->device = cfg.device;
     h->num_sms = prop.multiProcessorCount;
-    h->producers = cfg.producer_ctas ? cfg.producer_ctas : 16;
+    h->producers = cfg.producer_ctas;
     h->consumers = cfg.consumer_ctas;
     h->copy_mode = cfg.copy_mode;
+    h->slices = cfg.k_slices;
     if (cfg.wait_timeout_ns) h->timeout_ns = cfg.wait_timeout_ns;
 
     int prev_dev = 0;
@@ -207,12 +214,12 @@ TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
         const int n_blocks = static_cast<int>(ceil_div(cfg.max_rows, kBlockRows));
         Carve sizing{nullptr, 0};
         Ctrl tmp_ctrl{};
-        carve_ctrl(sizing, tmp_ctrl, n_chunks, n_blocks);
+        carve_ctrl(sizing, tmp_ctrl, n_chunks, n_blocks, h->slices);
         const size_t ctrl_bytes = sizing.off + 256;
         if ((e = cudaMalloc(&h->ctrl_mem, ctrl_bytes)) != cudaSuccess) { rc = TOVL_ERR_OOM; cudaGetLastError(); break; }
         if ((e = cudaMemset(h->ctrl_mem, 0, ctrl_bytes)) != cudaSuccess) { rc = cuda_fail(h, e, "memset"); break; }
         Carve cc{static_cast<char*>(h->ctrl_mem), 0};
-        carve_ctrl(cc, h->ctrl, n_chunks, n_blocks);
+        carve_ctrl(cc, h->ctrl, n_chunks, n_blocks, h->slices);
 
         const int E = cfg.max_experts > 0 ? cfg.max_experts : 1;
         h->max_seg = static_cast<int>(ceil_div(cfg.max_pairs > 0 ? cfg.max_pairs : 1, 1024));
@@ -297,18 +304,53 @@ static void base_params(tovl_ctx* h, FusedParams& p)
     std::memset(&p, 0, sizeof p);
     p.timeout_ns = h->timeout_ns;
     p.pipe_timeout_ns = pipe_timeout(h);
-    p.copy_mode = h->copy_mode;
     p.stats = h->stats;
     p.ctrl = h->ctrl;
 }
 
-static void split_ctas(tovl_ctx* h, int& P, int& C)
+// Producer / consumer CTA split for one call.  With no fixed producer count,
+// P balances the copy against the GEMM using per-SM rates measured for these
+// kernels on GB300 (about 60 GB/s of copy traffic per producer SM, about
+// 10 TFLOP/s per consumer SM), then grows while the consumers still finish
+// the tiles in the same number of waves (section 4 of the platform page: SMs
+// given to communication are taken from the GEMM, so the split is swept).
+static void split_ctas(tovl_ctx* h, int& P, int& C, long long tiles, double copy_bytes, double flops)
 {
-    P = h->producers;
-    if (P > h->num_sms - 1) P = h->num_sms - 1;
-    C = h->consumers ? h->consumers : h->num_sms - P;
-    if (C > h->num_sms - P) C = h->num_sms - P;
+    const int S = h->num_sms;
+    if (h->producers > 0) {
+        P = h->producers < S - 1 ? h->producers : S - 1;
+    } else {
+        const double tc = copy_bytes / 60e9, tg = flops / 10e12;
+        int p = static_cast<int>(S * tc / (tc + tg + 1e-30) + 0.5);
+        const int pmax = S / 4;
+        p = p < 4 ? 4 : (p > pmax ? pmax : p);
+        if (tiles > 0) {
+            const long long waves = (tiles + (S - p) - 1) / (S - p);
+            const int cmin = static_cast<int>((tiles + waves - 1) / waves);
+            if (S - cmin > p) p = S - cmin < pmax ? S - cmin : pmax;
+        }
+        P = p;
+    }
+    C = h->consumers ? h->consumers : S - P;
+    if (C > S - P) C = S - P;
     if (C < 1) C = 1;
+    h->last_P = P;
+    h->last_C = C;
+}
+
+// Slicing and producer-item geometry of one call: k_slices never exceeds the
+// K-blocks; an item moves item_rows rows of one slice, at most 8 KB per pass;
+// the producers' ordering group is the consumers' first wave of row blocks.
+static void call_geometry(const tovl_ctx* h, FusedParams& p, int C)
+{
+    p.k_slices = h->slices < p.n_kb ? h->slices : p.n_kb;
+    const int max_kbs = (p.n_kb + p.k_slices - 1) / p.k_slices;
+    const int n16 = max_kbs * kTileK * 2 / 16;
+    int ri = 64;
+    while (ri > 1 && ri * n16 > kItemInt4) ri >>= 1;
+    p.item_rows = ri;
+    p.wave_blocks = C > 0 ? (C + p.n_nb - 1) / p.n_nb : 1;
+    if (p.wave_blocks < 1) p.wave_blocks = 1;
 }
 
 static int reset_stats(tovl_ctx* h, cudaStream_t s)
@@ -338,7 +380,6 @@ static int check_gather(tovl_ctx* h, const void* const* shards, int S, int R, in
     if (static_cast<long long>(S) * R > h->cfg.max_rows) return TOVL_ERR_INVALID;
     for (int s = 0; s < S; ++s)
         if (!shards[s] || !aligned16(shards[s])) return TOVL_ERR_INVALID;
-    if (h->copy_mode == TOVL_COPY_BULK && K * 2 > 32768) return TOVL_ERR_UNSUPPORTED;
     return TOVL_OK;
 }
 
@@ -357,10 +398,12 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     p.n_nb = N / kTileN;
     p.row_bytes = K * 2;
     int P, C;
-    split_ctas(h, P, C);
+    split_ctas(h, P, C, static_cast<long long>((M + kTileM - 1) / kTileM) * p.n_nb, 4.0 * M * K,
+               2.0 * M * static_cast<double>(N) * K);
     p.n_producers = (flags & 1) ? P : 0;
     p.n_consumers = (flags & 2) ? C : 0;
     p.gated = (flags & 4) ? 1 : 0;
+    call_geometry(h, p, C);
     p.n_shards = S;
     p.rows_per_shard = R;
     for (int s = 0; s < S; ++s) p.shard[s] = shards ? shards[s] : nullptr;
@@ -435,7 +478,6 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     if (pairs > h->cfg.max_pairs) return TOVL_ERR_INVALID;
     const long long rows = tovl_dispatch_rows(T, k, E);
     if (rows > h->cfg.max_rows) return TOVL_ERR_INVALID;
-    if (h->copy_mode == TOVL_COPY_BULK && H * 2 > 32768) return TOVL_ERR_UNSUPPORTED;
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -465,10 +507,11 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.n_nb = N / kTileN;
     p.row_bytes = H * 2;
     int P, C;
-    split_ctas(h, P, C);
+    split_ctas(h, P, C, rows / kTileM * p.n_nb, 4.0 * pairs * H, 2.0 * pairs * static_cast<double>(N) * H);
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 1;
+    call_geometry(h, p, C);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;
     p.pad = h->plan.pad;
@@ -566,8 +609,8 @@ TOVL_API int tovl_sync_status(tovl_handle h)
 TOVL_API int tovl_ctrl_sizes(tovl_handle h, int* n_chunks, int* n_blocks)
 {
     if (!h) return TOVL_ERR_INVALID;
-    if (n_chunks) *n_chunks = h->ctrl.n_chunk_cap;
-    if (n_blocks) *n_blocks = h->ctrl.n_block_cap;
+    if (n_chunks) *n_chunks = h->ctrl.n_chunk_cap * h->ctrl.n_slices;
+    if (n_blocks) *n_blocks = h->ctrl.n_block_cap * h->ctrl.n_slices;
     return TOVL_OK;
 }
 
@@ -583,8 +626,8 @@ TOVL_API int tovl_read_ctrl(tovl_handle h, int* slots, int* cnts, int* rbcnts, l
     if (!h) return TOVL_ERR_INVALID;
     DeviceGuard g(h->device);
     int rc = sync_last(h);
-    const size_t nc = static_cast<size_t>(h->ctrl.n_chunk_cap) * sizeof(int);
-    const size_t nb = static_cast<size_t>(h->ctrl.n_block_cap) * sizeof(int);
+    const size_t nc = static_cast<size_t>(h->ctrl.n_chunk_cap) * h->ctrl.n_slices * sizeof(int);
+    const size_t nb = static_cast<size_t>(h->ctrl.n_block_cap) * h->ctrl.n_slices * sizeof(int);
     if (rc == TOVL_OK) rc = d2h(h, slots, h->ctrl.slot, nc);
     if (rc == TOVL_OK) rc = d2h(h, cnts, h->ctrl.cnt, nc);
     if (rc == TOVL_OK) rc = d2h(h, rbcnts, h->ctrl.rbcnt, nb);
@@ -673,12 +716,11 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
 TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
 {
     if (!h || !value) return TOVL_ERR_INVALID;
-    int P, C;
-    split_ctas(h, P, C);
     switch (option) {
-    case 1: *value = P; return TOVL_OK;
-    case 2: *value = C; return TOVL_OK;
+    case 1: *value = h->last_P; return TOVL_OK;
+    case 2: *value = h->last_C; return TOVL_OK;
     case 3: *value = h->copy_mode; return TOVL_OK;
+    case 9: *value = h->slices; return TOVL_OK;
     case 4: *value = h->stats; return TOVL_OK;
     case 5: *value = h->timeout_ns; return TOVL_OK;
     case 6: *value = h->copy_ctas; return TOVL_OK;

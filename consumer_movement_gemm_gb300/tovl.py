@@ -32,6 +32,7 @@ OPT_TIMEOUT_NS = 5
 OPT_COPY_CTAS = 6
 OPT_COPY_WAITERS = 7
 OPT_FAULT_GATE_OFFSET = 8
+OPT_K_SLICES = 9
 
 
 class TovlError(RuntimeError):
@@ -55,6 +56,7 @@ class tovl_config(ctypes.Structure):
         ("max_rows", ctypes.c_longlong),
         ("max_pairs", ctypes.c_int),
         ("max_experts", ctypes.c_int),
+        ("k_slices", ctypes.c_int),
     ]
 
 

@@ -53,7 +53,8 @@ typedef enum {
     TOVL_ERR_OOM = 5           /* device allocation failed in tovl_create */
 } tovl_status;
 
-/* Row-copy mechanism of the producers. */
+/* Row-copy mechanism of tovl_gated_copy.  The producers of the fused
+ * kernels always use 16-byte vector copies by 12 warps per CTA. */
 typedef enum {
     TOVL_COPY_VECTOR = 0,      /* 16-byte vector loads/stores by warps */
     TOVL_COPY_BULK = 1         /* bulk asynchronous copies through a shared-memory ring */
@@ -63,13 +64,19 @@ typedef struct {
     int device;                /* CUDA device ordinal */
     int chunk_rows;            /* watermark chunk; must be 64 (or 0 for 64) -- section 4 */
     int gate_rows;             /* GEMM row-block gate; must be 128 (or 0 for 128) -- section 5 */
-    int producer_ctas;         /* P; 0 = 16 */
+    int producer_ctas;         /* P; 0 = chosen per call: copy and GEMM time balanced,
+                                  then grown while the GEMM keeps its wave count */
     int consumer_ctas;         /* C; 0 = all remaining SMs */
     long long wait_timeout_ns; /* bound of every device wait; 0 = 2 s */
-    int copy_mode;             /* tovl_copy_mode */
+    int copy_mode;             /* tovl_copy_mode of tovl_gated_copy */
     long long max_rows;        /* capacity in rows of gathered/dispatched buffers and copies */
     int max_pairs;             /* largest T*k of a dispatch call */
     int max_experts;           /* largest E of a dispatch call (<= 512) */
+    int k_slices;              /* 1..8 (0 = 1): each 64-row chunk watermark (and each
+                                  128-row block counter) is split into this many
+                                  K-ranges, published separately, so a GEMM tile may
+                                  start on the first K-range of its rows; 1 = one
+                                  watermark per chunk (sections 4-5 exactly) */
 } tovl_config;
 
 /* Fills `cfg` with defaults for `device`. */
@@ -161,11 +168,14 @@ int tovl_gated_copy(tovl_handle h, const void* src, void* dst, long long n_rows,
  * (TOVL_OK if none) and clears it. */
 int tovl_sync_status(tovl_handle h);
 
-/* Number of chunk slots/counters and row-block counters of the handle. */
+/* Lengths of the control-plane arrays: chunk slots/counters
+ * (max_rows/64 chunks x k_slices, index chunk*k_slices + slice) and
+ * row-block counters (max_rows/128 blocks x k_slices). */
 int tovl_ctrl_sizes(tovl_handle h, int* n_chunks, int* n_blocks);
 
 /* Copies the control plane to host arrays (after synchronising): slots and
- * cnts [n_chunks], rbcnts [n_blocks]; *seq = calls that were protocol rounds.
+ * cnts [n_chunks], rbcnts [n_blocks] (lengths from tovl_ctrl_sizes);
+ * *seq = calls that were protocol rounds.
  * Any pointer may be NULL. */
 int tovl_read_ctrl(tovl_handle h, int* slots, int* cnts, int* rbcnts, long long* seq);
 
@@ -177,7 +187,8 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
 
 /* Options for sweeps: 1 = producer CTAs, 2 = consumer CTAs, 3 = copy mode,
  * 4 = statistics on/off, 5 = wait timeout in ns, 6 = copy-sweep CTAs,
- * 7 = copy-sweep waiter CTAs, 8 = fault injection for tests: consumer gates
+ * 7 = copy-sweep waiter CTAs, 9 = k_slices (read only),
+ * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in
  * the status word (0 = off). */

@@ -14,7 +14,7 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 # functions that run after the role split: no CTA-wide barrier may appear
 ROLE_FUNCTIONS = {
-    "fused.cu": ["consumer_tma", "consumer_mma", "consumer_epilogue", "seed_counters", "producer_v4"],
+    "fused.cu": ["consumer_tma", "consumer_mma", "consumer_epilogue", "gate", "seed_counters", "copy_item"],
     "copyplane.cuh": ["bulk_stream", "run_bulk"],
     "copy.cu": ["copy_v4", "copy_waiter", "copy_seeds"],
 }

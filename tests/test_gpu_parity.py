@@ -80,10 +80,10 @@ def _gather_round(h, cfg, seed):
     return X, W, gathered, out
 
 
-@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
-def test_tiny_gather_gemm_three_rounds(copy_mode):
+@pytest.mark.parametrize("k_slices", [1, 2, 4, 8])
+def test_tiny_gather_gemm_three_rounds(k_slices):
     cfg = workloads.TINY
-    with _handle(copy_mode=copy_mode) as h:
+    with _handle(k_slices=k_slices) as h:
         for r in range(1, cfg.rounds + 1):
             X, W, gathered, out = _gather_round(h, cfg, workloads.round_seed(cfg.seed, r))
             assert h.sync_status() == 0
@@ -94,10 +94,11 @@ def test_tiny_gather_gemm_three_rounds(copy_mode):
             _check_ctrl(h, r)
 
 
-@pytest.mark.parametrize("S,R,K,N,P", [(3, 100, 192, 256, 4), (1, 64, 64, 512, 1), (5, 77, 128, 256, 32)])
-def test_gather_gemm_ragged(S, R, K, N, P):
+@pytest.mark.parametrize("S,R,K,N,P,KS", [(3, 100, 192, 256, 4, 2), (1, 64, 64, 512, 1, 4), (5, 77, 128, 256, 32, 1),
+                                          (2, 200, 320, 256, 8, 4), (7, 33, 448, 512, 3, 8)])
+def test_gather_gemm_ragged(S, R, K, N, P, KS):
     cfg = workloads.GatherCfg("ragged", S, R, K, N, rounds=2)
-    with _handle(producer_ctas=P) as h:
+    with _handle(producer_ctas=P, k_slices=KS) as h:
         for r in range(1, 3):
             X, W, gathered, out = _gather_round(h, cfg, 100 + r)
             assert h.sync_status() == 0
@@ -107,10 +108,10 @@ def test_gather_gemm_ragged(S, R, K, N, P):
             _check_ctrl(h, r)
 
 
-@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
-def test_copy_only_control(copy_mode):
+@pytest.mark.parametrize("k_slices", [1, 4])
+def test_copy_only_control(k_slices):
     cfg = workloads.GatherCfg("copy", 4, 96, 256, 256, rounds=2)
-    with _handle(copy_mode=copy_mode) as h:
+    with _handle(k_slices=k_slices) as h:
         for r in range(1, 3):
             X, _ = workloads.gather_inputs(cfg, r, DEV)
             gathered = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device=DEV)
@@ -122,7 +123,7 @@ def test_copy_only_control(copy_mode):
 
 def test_timeout_is_reported_and_handle_recovers():
     cfg = workloads.TINY
-    with _handle(wait_timeout_ns=5_000_000) as h:
+    with _handle(wait_timeout_ns=5_000_000, k_slices=2) as h:
         h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # gates wait for a sequence nobody publishes
         _gather_round(h, cfg, 1)
         assert h.sync_status() == tovl.TOVL_ERR_TIMEOUT
@@ -180,10 +181,10 @@ ROUTINGS = {
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
-@pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_BULK, tovl.TOVL_COPY_VECTOR])
-def test_dispatch_grouped_gemm_small(routing, copy_mode):
+@pytest.mark.parametrize("k_slices", [1, 2])
+def test_dispatch_grouped_gemm_small(routing, k_slices):
     H, N = 192, 256
-    with _handle(copy_mode=copy_mode) as h:
+    with _handle(k_slices=k_slices) as h:
         for r in range(1, 4):
             topk_np, E = ROUTINGS[routing](workloads.round_seed(1, r))
             T = topk_np.shape[0]
@@ -216,7 +217,7 @@ def test_dispatch_bad_expert_id_is_a_noop_round():
 @pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK])
 def test_gated_copy_small(row_bytes, copy_mode):
     n = 5000
-    with _handle(copy_mode=copy_mode, max_rows=n) as h:
+    with _handle(copy_mode=copy_mode, max_rows=n, k_slices=2) as h:
         for r in range(1, 3):
             perm_np = workloads.permutation(n, r)
             src = workloads.random_bytes(n, row_bytes, r, DEV)
