@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip the extra workloads")
     ap.add_argument("--full", action="store_true", help="extra workloads at their full round counts")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", choices=["fused", "gemm", "copy", "dispatch"], default=None,
+                    help="run only W + K calls of one kernel on a small case (for ncu captures) and exit")
     return ap.parse_args(argv)
 
 
@@ -242,13 +244,23 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU legs
 class Timer:
-    """CUDA-event timing of single calls on one stream, L2 flushed before each."""
+    """CUDA-event timing of single calls on one stream, L2 flushed before each.
+
+    The flush writes a 512 MiB buffer (evicting everything the call used) and
+    then reads another 512 MiB buffer, so the L2 is left holding clean lines
+    of neither the inputs nor the flush writes: the timed call starts cold
+    and does not pay for writing back the flush buffer's dirty lines."""
 
     def __init__(self, stream):
         import torch
         self.torch = torch
         self.stream = stream
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def do_flush(self):
+        self.flush.fill_(1)
+        self.flush_read.max()
 
     def time_calls(self, fn, n: int, flush: bool = True):
         torch = self.torch
@@ -256,7 +268,7 @@ class Timer:
         with torch.cuda.stream(self.stream):
             for a, b in evs:
                 if flush:
-                    self.flush.fill_(1)
+                    self.do_flush()
                 a.record(self.stream)
                 fn()
                 b.record(self.stream)
@@ -473,7 +485,7 @@ def run_tovl(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "shards": cfg.shards, "rows_per_shard": cfg.rows_per_shard, "K": cfg.K,
                    "N": cfg.N, "parallelism": "replicas only" if world > 1 else "single GPU",
-                   "l2": "flushed (512 MiB write) before every timed step",
+                   "l2": "flushed before every timed step: 512 MiB written, then 512 MiB read (cold, clean L2)",
                    "producer_ctas": acc["producer_ctas"], "consumer_ctas": acc["consumer_ctas"],
                    "k_slices": args.k_slices},
         "overlap_efficiency": acc["overlap_efficiency"],
@@ -493,9 +505,60 @@ def run_tovl(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Small, deterministic launch sequences for profiler captures: W + K
+    calls of one kernel, nothing else timed.
+      fused     tovl_gather_gemm on the TP shape (about 110 MB resident)
+      gemm      tovl_gemm_only on the TP shape
+      copy      tovl_gated_copy, 2^18 rows x 8 KB, gated (4 GB resident)
+      dispatch  tovl_dispatch_grouped_gemm on the uniform top-2 workload"""
+    import torch
+    import workloads
+    from consumer_movement_gemm_gb300 import build as tovl_build
+    from consumer_movement_gemm_gb300 import tovl
+    tovl_build.build()
+    dev = "cuda"
+    n = args.warmup + args.steps
+    if args.profile in ("fused", "gemm"):
+        cfg = workloads.TP
+        with tovl.Handle(0, max_rows=1 << 14, producer_ctas=args.producers, k_slices=args.k_slices) as h:
+            X, W, gathered, out = tp_setup(h, cfg, dev)
+            for _ in range(n):
+                if args.profile == "fused":
+                    h.gather_gemm(X, W, gathered, out)
+                else:
+                    h.gemm_only(gathered, W, out)
+            assert h.sync_status() == 0
+    elif args.profile == "copy":
+        rows, rb = 1 << 18, 8192
+        perm = torch.from_numpy(workloads.permutation(rows, 0)).to(dev)
+        src = workloads.random_bytes(rows, rb, 0, dev)
+        dst = torch.empty_like(src)
+        with tovl.Handle(0, max_rows=rows, copy_mode=tovl.TOVL_COPY_VECTOR) as h:
+            for _ in range(n):
+                h.gated_copy(src, dst, perm, gated=True)
+            assert h.sync_status() == 0
+    else:
+        cfg = workloads.DISPATCH
+        x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
+        rows = tovl.dispatch_rows(cfg.T, cfg.k, cfg.E)
+        with tovl.Handle(0, max_rows=rows, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=args.k_slices) as h:
+            topk = torch.from_numpy(topk_np).to(dev)
+            dispatched = torch.zeros(rows, cfg.H, dtype=torch.bfloat16, device=dev)
+            offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+            out = torch.empty(rows, cfg.N, dtype=torch.bfloat16, device=dev)
+            for _ in range(n):
+                h.dispatch_grouped_gemm(x, topk, W, dispatched, offs, out)
+            assert h.sync_status() == 0
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "calls": n}))
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_tovl(args)

@@ -19,13 +19,16 @@ constexpr int kTileN = 256;
 constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 384;      // 12 warps: TMA, MMA, 8 x epilogue, 2 idle (consumers) / 12 copy warps (producers)
+constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 5 idle (consumers) / 16 copy warps (producers)
 constexpr int kEpiWarp0 = 2;       // first epilogue warp
 constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each owning 128 of the 256 columns
+constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
+constexpr int kTraceCap = 1 << 20; // timeline entries kept when statistics are on
 constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
 constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)
 constexpr int kReleaseBatch = 4;   // producer items per batched release
 constexpr int kMaxShards = 64;
+constexpr int kMaxK = 32768;       // a producer ring stage must hold one 64 KB row
 constexpr int kMaxExperts = 512;
 
 constexpr int kStageA = kTileM * kTileK * 2;      // 16 KB
@@ -63,8 +66,10 @@ struct Ctrl {
     int* status;          // [1] sticky error code
     int* abort_seq;       // [1] highest sequence that gave up waiting
     unsigned long long* stats;   // [kNumStats]
-    long long* pub_ns;    // [n_chunk_cap]  publish time of each chunk (copy sweep)
-    long long* obs_ns;    // [n_chunk_cap]  first observation time by a waiter
+    long long* pub_ns;    // [n_chunk_cap * n_slices]  publish time of each chunk slice (stats / stamps)
+    long long* obs_ns;    // [n_chunk_cap]  first observation time by a waiter (copy sweep)
+    long long* trace;     // [trace_cap]  fused kernel timeline: gate-pass times per tile slice, then tile end times
+    int trace_cap;
     int n_chunk_cap;
     int n_block_cap;
     int n_slices;         // K-slices per chunk / block; slot, cnt and rbcnt hold n_slices entries per chunk / block
@@ -106,6 +111,7 @@ struct FusedParams {
     int k_slices;         // K-slices in use this call (<= ctrl.n_slices); slices beyond are seeded
     int wave_blocks;      // row blocks the consumers' first wave covers (producer ordering group)
     int item_rows;        // rows per producer item (a power of two dividing 64)
+    int trace_tiles;      // tile count bound that lays out the timeline (gate times, then end times)
     // gather sources
     const void* shard[kMaxShards];
     int n_shards;

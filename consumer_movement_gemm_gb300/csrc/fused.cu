@@ -73,6 +73,7 @@ struct ConsumerSmem {
     uint64_t* tfull;     // MMA -> epilogue (per accumulator)
     uint64_t* tempty;    // epilogue -> MMA
     uint32_t* tmem_slot;
+    int* gates_passed;   // gate warp -> TMA warp: number of (tile, slice) gates passed
 };
 
 __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t* smem)
@@ -86,7 +87,13 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t* smem)
     s.tfull = bars + 2 * kStages;
     s.tempty = bars + 2 * kStages + 2;
     s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    s.gates_passed = reinterpret_cast<int*>(bars + 2 * kStages + 5);
     return s;
+}
+
+__device__ __forceinline__ void trace_put(const FusedParams& p, long long idx, unsigned long long v)
+{
+    if (p.stats && idx < p.ctrl.trace_cap) p.ctrl.trace[idx] = static_cast<long long>(v);
 }
 
 // Gate: the rows of row block mb, K-slice s, are complete this round.
@@ -106,33 +113,71 @@ __device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb,
         target = p.gate_seq * kBlockRows;
     }
     const int r = warp_wait_ge(words, n, target, p.ctrl, p.seq, p.timeout_ns);
-    // the rows were written through the generic proxy; order them before
-    // this thread's tensor-memory-access (async proxy) reads
-    if (ptx::lane_id() == 0) ptx::fence_proxy_async_global();
     return static_cast<unsigned long long>(r < 0 ? -r : r);
 }
 
-// TMA warp: per tile and K-slice, gate the slice's rows, then stream A and B
-// k-blocks into the stage ring.
-__device__ void consumer_tma(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles)
+// Gate warp: walks the consumer's (tile, slice) schedule ahead of the TMA
+// warp, waits for each slice's rows on the protocol (acquire polls of the
+// local slots / counters) and hands every passed gate to the TMA warp with a
+// CTA-scope release of the running count.  A gate that times out is handed
+// on as well, so the pipeline drains; the status word holds the error.
+__device__ void consumer_gate(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles)
 {
     const uint32_t lane = ptx::lane_id();
-    uint32_t stage = 0, phase = 0;
     unsigned long long polls = 0;
-    int fail = 0;
-    for (int t = cid; t < n_tiles && !fail; t += p.n_consumers) {
+    int passed = 0;
+    for (int t = cid; t < n_tiles; t += p.n_consumers) {
+        const int mb = t / p.n_nb;
+        for (int sl = 0; sl < p.k_slices; ++sl) {
+            polls += gate(p, mb, sl);
+            ++passed;
+            if (lane == 0) {
+                ptx::st_release_cta_smem(s.gates_passed, passed);
+                trace_put(p, static_cast<long long>(t) * p.k_slices + sl, ptx::globaltimer());
+            }
+            __syncwarp();
+        }
+    }
+    if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
+}
+
+// TMA lane: wait until the gate warp has passed gate number `idx` (bounded).
+__device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem& s, int idx)
+{
+    if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+            record_error(p.ctrl, kErrTimeout);
+            return false;
+        }
+        __nanosleep(20);
+    }
+}
+
+// TMA warp: per tile and K-slice, wait for the slice's gate, then stream A
+// and B k-blocks into the stage ring.  One lane issues everything.
+__device__ void consumer_tma(const FusedParams& p, const ConsumerSmem& s, int cid, int n_tiles)
+{
+    if (ptx::lane_id() != 0) return;
+    uint32_t stage = 0, phase = 0;
+    int gate_idx = 0;
+    for (int t = cid; t < n_tiles; t += p.n_consumers) {
         const int mb = t / p.n_nb;
         const int nb = t % p.n_nb;
         const int brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
-        for (int sl = 0; sl < p.k_slices && !fail; ++sl) {
-            if (p.gated) polls += gate(p, mb, sl);
-            if (lane == 0) {
+        for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
+            if (p.gated) {
+                if (!wait_gate(p, s, gate_idx)) return;
+                // the rows were written through the generic proxy; order them
+                // before this thread's tensor-memory-access (async proxy) reads
+                ptx::fence_proxy_async_global();
+            }
+            {
                 const int kb1 = kb_begin(p, sl + 1);
                 for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) {
-                        fail = 1;
-                        break;
-                    }
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
                     ptx::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
                     ptx::tma_load_2d(s.a + stage * kStageA, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
                     uint8_t* bdst = s.b + stage * kStageB;
@@ -146,10 +191,8 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem& s, int ci
                     }
                 }
             }
-            fail = __shfl_sync(0xffffffffu, fail, 0);
         }
     }
-    if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
 }
 
 // MMA warp: one lane issues tcgen05.mma into a double-buffered TMEM
@@ -235,6 +278,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem& s, i
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&s.tempty[acc]);
+        if (p.stats && lane == 0) {
+            const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
+            if (idx < p.ctrl.trace_cap)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
     }
 }
 
@@ -251,6 +299,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
             ptx::mbar_init(&s.tfull[i], 1);
             ptx::mbar_init(&s.tempty[i], kEpiWarps * 32);
         }
+        *s.gates_passed = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
         ptx::prefetch_tmap(&p.tmap_b);
@@ -270,6 +319,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     if (warp == 0) consumer_tma(p, s, cid, n_tiles);
     else if (warp == 1) consumer_mma(p, s, cid, n_tiles, tmem_base);
     else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue(p, s, cid, n_tiles, tmem_base, valid_rows);
+    else if (warp == kGateWarp && p.gated) consumer_gate(p, s, cid, n_tiles);
     __syncwarp();
 
     // teardown: full-CTA barrier 0, after every role has finished
@@ -322,15 +372,25 @@ __device__ __forceinline__ const uint8_t* row_src(const FusedParams& p, int r)
 // Counter index and completion of an item's rows.
 __device__ __forceinline__ void item_done(const FusedParams& p, int counter, int n)
 {
-    if (p.mode == kModeGather) arrive_and_publish(p.ctrl, counter, n, p.seq);
-    else ptx::red_add_release_gpu(p.ctrl.rbcnt + counter, n);
+    if (p.mode == kModeGather) {
+        if (arrive_and_publish(p.ctrl, counter, n, p.seq) && p.stats)
+            p.ctrl.pub_ns[counter] = static_cast<long long>(ptx::globaltimer());
+    } else {
+        ptx::red_add_release_gpu(p.ctrl.rbcnt + counter, n);
+    }
 }
 
 // Per-round padding seeds.  Each counter must gain exactly its per-round
 // quota (64 per chunk slice, 128 per block slice) every call, so whatever
 // this call does not fill -- rows past the end, padding rows, slices beyond
 // k_slices, blocks beyond this round -- is added as one seed.
-__device__ void seed_counters(const FusedParams& p, int gw, int n_gw)
+// Seeds come in two phases.  Completion seeds -- the padding of a partial
+// chunk or of a dispatch row block -- are part of a gate's target, so they
+// are added before any row is copied.  Quota seeds -- counters this call
+// does not use at all (chunks past the rows, slices past k_slices, the other
+// counter family) -- only keep the closed form, so they are added after the
+// copies, off the consumers' critical path.
+__device__ void seed_counters(const FusedParams& p, int gw, int n_gw, bool completion)
 {
     const uint32_t lane = ptx::lane_id();
     const Ctrl& c = p.ctrl;
@@ -338,25 +398,27 @@ __device__ void seed_counters(const FusedParams& p, int gw, int n_gw)
     // chunk-slice counters
     for (int cs = gw * 32 + lane; cs < c.n_chunk_cap * S; cs += n_gw * 32) {
         const int ch = cs / S, sl = cs - ch * S;
-        int seed = kChunkRows;
-        if (p.mode == kModeGather && sl < p.k_slices) seed = kChunkRows - min(max(p.M - ch * kChunkRows, 0), kChunkRows);
-        if (seed > 0) arrive_and_publish(c, cs, seed, p.seq);
+        int real = 0;
+        if (p.mode == kModeGather && sl < p.k_slices) real = min(max(p.M - ch * kChunkRows, 0), kChunkRows);
+        const bool is_completion = real > 0 && real < kChunkRows;
+        if (is_completion == completion && real < kChunkRows) arrive_and_publish(c, cs, kChunkRows - real, p.seq);
     }
     // block-slice counters
     if (p.mode == kModeGather) {
-        for (int bs = gw * 32 + lane; bs < c.n_block_cap * S; bs += n_gw * 32)
-            ptx::red_add_release_gpu(c.rbcnt + bs, kBlockRows);
+        if (!completion)
+            for (int bs = gw * 32 + lane; bs < c.n_block_cap * S; bs += n_gw * 32)
+                ptx::red_add_release_gpu(c.rbcnt + bs, kBlockRows);
         return;
     }
     const int n_blocks = p.meta[1];
     const int zero = p.meta[2];
     for (int b = gw; b < c.n_block_cap; b += n_gw) {
         if (b >= n_blocks) {
-            if (static_cast<int>(lane) < S) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, kBlockRows);
+            if (!completion && static_cast<int>(lane) < S) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, kBlockRows);
             continue;
         }
         const int pad = p.pad[b];
-        if (zero && pad > 0) {
+        if (completion && zero && pad > 0) {
             // padding rows are the last `pad` rows of the block; they must be
             // zero before the counters reach their target
             int4* d = reinterpret_cast<int4*>(static_cast<uint8_t*>(p.gathered) +
@@ -366,16 +428,19 @@ __device__ void seed_counters(const FusedParams& p, int gw, int n_gw)
             for (size_t i = lane; i < n16; i += 32) ptx::st_v4(d + i, z);
             __syncwarp();
         }
-        // slices beyond k_slices get the whole block quota, the others the padding count
+        // slices in use get the padding count (completion), slices beyond
+        // k_slices the whole block quota (quota)
         if (static_cast<int>(lane) < S) {
-            const int seed = static_cast<int>(lane) < p.k_slices ? pad : kBlockRows;
-            if (seed > 0) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, seed);
+            const bool used = static_cast<int>(lane) < p.k_slices;
+            const int seed = used ? pad : kBlockRows;
+            if (used == completion && seed > 0) ptx::red_add_release_gpu(c.rbcnt + b * S + lane, seed);
         }
     }
 }
 
 // Copy one item: item_rows destination rows x the K-slice's bytes, as one
-// flat range of 16-byte words, up to 16 per lane in flight.
+// flat range of 16-byte words walked 32 words per step, 16 words per lane in
+// flight.  A per-warp table in shared memory holds each row's source.
 __device__ __forceinline__ int copy_item(const FusedParams& p, const Item& it, const uint8_t** tbl)
 {
     const uint32_t lane = ptx::lane_id();
@@ -385,8 +450,8 @@ __device__ __forceinline__ int copy_item(const FusedParams& p, const Item& it, c
     const size_t soff = static_cast<size_t>(kb_begin(p, it.s)) * kTileK * 2;
     const int n16 = (kb_begin(p, it.s + 1) - kb_begin(p, it.s)) * kTileK * 2 / 16;
     uint8_t* dst = static_cast<uint8_t*>(p.gathered) + soff + static_cast<size_t>(it.r0) * p.row_bytes;
-    // lane position (row, col) in the item's flat range of 16-byte words,
-    // advanced by 32 words per step without division
+    // lane position (row, col) in the item's flat range, advanced by 32 words
+    // per step without division
     int row = static_cast<int>(lane) / n16;
     int col = static_cast<int>(lane) - row * n16;
     while (row < RI) {
@@ -436,13 +501,16 @@ __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
     const int gw = pid * n_warps + warp;
     const int n_gw = p.n_producers * n_warps;
     if (threadIdx.x == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
-    seed_counters(p, gw, n_gw);
+    seed_counters(p, gw, n_gw, true);
 
     const uint8_t** tbl = reinterpret_cast<const uint8_t**>(smem) + warp * 64;   // row-source table per warp
     const int n_blocks = num_row_blocks(p);
     const int n_items = n_blocks * p.k_slices * (kBlockRows / p.item_rows);
     const int S = p.ctrl.n_slices;
-    // lane j < kReleaseBatch holds the j-th pending item of the batch
+    // Items of the consumers' first wave are released one by one (their
+    // consumers are already waiting); later items in batches, which saves
+    // release fences.  Lane j < kReleaseBatch holds the batch's j-th item.
+    const int first_wave_items = p.wave_blocks * p.k_slices * (kBlockRows / p.item_rows);
     int pend_counter = 0, pend_n = 0, n_pend = 0;
     for (int i = gw; i < n_items; i += n_gw) {
         const Item it = decode_item(p, i, n_blocks);
@@ -452,7 +520,7 @@ __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
             pend_counter = counter;
             pend_n = n;
         }
-        if (++n_pend == kReleaseBatch) {
+        if (++n_pend == kReleaseBatch || i < first_wave_items) {
             // the copies above happen-before every lane's release below
             __syncwarp();
             if (static_cast<int>(lane) < n_pend && pend_n > 0) item_done(p, pend_counter, pend_n);
@@ -461,6 +529,8 @@ __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
     }
     __syncwarp();
     if (static_cast<int>(lane) < n_pend && pend_n > 0) item_done(p, pend_counter, pend_n);
+    __syncwarp();
+    seed_counters(p, gw, n_gw, false);
     __syncwarp();
     __syncthreads();
     if (threadIdx.x == 0) stat_max(p, kStatProdEndNs, ptx::globaltimer());

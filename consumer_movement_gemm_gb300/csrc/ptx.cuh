@@ -95,6 +95,19 @@ __device__ __forceinline__ int atom_max_relaxed_gpu(int* p, int v)
     return old;
 }
 
+// CTA-scope release/acquire on a shared-memory word (hand-off between warps).
+__device__ __forceinline__ void st_release_cta_smem(int* p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta_smem(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu()
 {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");

@@ -46,6 +46,8 @@ struct tovl_ctx {
     cudaStream_t last_stream = nullptr;
     const void* last_dispatched = nullptr;
     int last_T = 0, last_k = 0, last_E = 0;
+    long long last_tiles = 0;    // tiles and K-slices of the last fused call (trace layout)
+    int last_ks = 0;
     EncodeTiledFn encode = nullptr;
     char last_error[256] = {0};
 };
@@ -137,8 +139,10 @@ static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks, int S)
     ctrl.status = c.take<int>(1);
     ctrl.abort_seq = c.take<int>(1);
     ctrl.stats = c.take<unsigned long long>(kNumStats);
-    ctrl.pub_ns = c.take<long long>(n_chunks);
+    ctrl.pub_ns = c.take<long long>(static_cast<size_t>(n_chunks) * S);
     ctrl.obs_ns = c.take<long long>(n_chunks);
+    ctrl.trace = c.take<long long>(kTraceCap);
+    ctrl.trace_cap = kTraceCap;
     ctrl.n_chunk_cap = n_chunks;
     ctrl.n_block_cap = n_blocks;
     ctrl.n_slices = S;
@@ -353,11 +357,19 @@ static void call_geometry(const tovl_ctx* h, FusedParams& p, int C)
     if (p.wave_blocks < 1) p.wave_blocks = 1;
 }
 
-static int reset_stats(tovl_ctx* h, cudaStream_t s)
+static int reset_stats(tovl_ctx* h, cudaStream_t s, long long tiles, int ks)
 {
+    h->last_tiles = tiles;
+    h->last_ks = ks;
     if (!h->stats) return TOVL_OK;
-    // min slots start at all-ones, the others at zero
+    // min slots start at all-ones, the others at zero; the timeline at zero
     cudaError_t e = cudaMemsetAsync(h->ctrl.stats, 0, kNumStats * sizeof(unsigned long long), s);
+    long long n_trace = tiles * (ks + 1);
+    if (n_trace > h->ctrl.trace_cap) n_trace = h->ctrl.trace_cap;
+    if (e == cudaSuccess && n_trace > 0) e = cudaMemsetAsync(h->ctrl.trace, 0, n_trace * sizeof(long long), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(h->ctrl.pub_ns, 0,
+                            static_cast<size_t>(h->ctrl.n_chunk_cap) * h->ctrl.n_slices * sizeof(long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ctrl.stats + kStatConsStartNs, 0xff, sizeof(unsigned long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ctrl.stats + kStatProdStartNs, 0xff, sizeof(unsigned long long), s);
     return e == cudaSuccess ? TOVL_OK : cuda_fail(h, e, "stats reset");
@@ -377,6 +389,7 @@ struct DeviceGuard {
 static int check_gather(tovl_ctx* h, const void* const* shards, int S, int R, int K)
 {
     if (!shards || S < 1 || S > kMaxShards || R < 1 || K < kTileK || K % kTileK) return TOVL_ERR_INVALID;
+    if (K > kMaxK) return TOVL_ERR_UNSUPPORTED;
     if (static_cast<long long>(S) * R > h->cfg.max_rows) return TOVL_ERR_INVALID;
     for (int s = 0; s < S; ++s)
         if (!shards[s] || !aligned16(shards[s])) return TOVL_ERR_INVALID;
@@ -419,7 +432,8 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     if (round) p.seq = static_cast<int>(h->seq + 1);
     else p.seq = static_cast<int>(h->seq);
     p.gate_seq = p.seq + h->fault_gate_offset;
-    if ((rc = reset_stats(h, stream)) != TOVL_OK) return rc;
+    p.trace_tiles = (flags & 2) ? ((M + kTileM - 1) / kTileM) * p.n_nb : 0;
+    if ((rc = reset_stats(h, stream, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
     const cudaError_t e = launch_fused(p, stream, (flags & 4) != 0);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
     if (round) h->seq += 1;
@@ -473,6 +487,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
         return TOVL_ERR_INVALID;
     if (T < 0 || k < 1 || E < 1 || E > h->cfg.max_experts || E > kMaxExperts) return TOVL_ERR_INVALID;
     if (H < kTileK || H % kTileK) return TOVL_ERR_INVALID;
+    if (H > kMaxK) return TOVL_ERR_UNSUPPORTED;
     if (N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
     const long long pairs = static_cast<long long>(T) * k;
     if (pairs > h->cfg.max_pairs) return TOVL_ERR_INVALID;
@@ -528,7 +543,8 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
         return rc;
     p.seq = static_cast<int>(h->seq + 1);
     p.gate_seq = p.seq + h->fault_gate_offset;
-    if ((rc = reset_stats(h, s)) != TOVL_OK) return rc;
+    p.trace_tiles = static_cast<int>(rows / kTileM * p.n_nb);
+    if ((rc = reset_stats(h, s, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
     e = launch_fused(p, s, true);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
     h->seq += 1;
@@ -660,6 +676,32 @@ TOVL_API int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n)
     int rc = sync_last(h);
     if (n > kNumStats) n = kNumStats;
     if (rc == TOVL_OK) rc = d2h(h, stats, h->ctrl.stats, static_cast<size_t>(n) * sizeof(unsigned long long));
+    return rc;
+}
+
+TOVL_API int tovl_read_trace(tovl_handle h, int what, long long* out, long long n)
+{
+    if (!h || !out || n < 0) return TOVL_ERR_INVALID;
+    const long long* src = nullptr;
+    long long avail = 0;
+    if (what == 0) {
+        src = h->ctrl.pub_ns;
+        avail = static_cast<long long>(h->ctrl.n_chunk_cap) * h->ctrl.n_slices;
+    } else if (what == 1) {
+        src = h->ctrl.trace;
+        avail = h->last_tiles * h->last_ks;
+    } else if (what == 2) {
+        src = h->ctrl.trace + h->last_tiles * h->last_ks;
+        avail = h->last_tiles;
+    } else {
+        return TOVL_ERR_INVALID;
+    }
+    if (src - h->ctrl.trace >= 0 && (src - h->ctrl.trace) + avail > h->ctrl.trace_cap)
+        avail = h->ctrl.trace_cap - (src - h->ctrl.trace);
+    if (n > avail) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    int rc = sync_last(h);
+    if (rc == TOVL_OK) rc = d2h(h, out, src, static_cast<size_t>(n) * sizeof(long long));
     return rc;
 }
 

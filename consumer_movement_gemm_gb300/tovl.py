@@ -85,6 +85,7 @@ SIGNATURES = {
     "tovl_get_option": ([_P, _I, _LLP], _I),
     "tovl_read_stats": ([_P, _ULLP, _I], _I),
     "tovl_read_latency": ([_P, _P, _P, _I], _I),
+    "tovl_read_trace": ([_P, _I, _P, _LL], _I),
     "tovl_num_sms": ([_P], _I),
     "tovl_error_string": ([_I], ctypes.c_char_p),
     "tovl_last_error": ([_P], ctypes.c_char_p),
@@ -267,6 +268,12 @@ class Handle:
         rc = load().tovl_read_latency(self.h, pub.ctypes.data, obs.ctypes.data, n)
         _check(self.h, rc, "tovl_read_latency")
         return pub, obs
+
+    def read_trace(self, what: int, n: int):
+        import numpy as np
+        out = np.zeros(n, np.int64)
+        _check(self.h, load().tovl_read_trace(self.h, what, out.ctypes.data, n), "tovl_read_trace")
+        return out
 
     @property
     def num_sms(self) -> int:

@@ -99,7 +99,7 @@ int tovl_destroy(tovl_handle h);
  *   shards      host array of S device pointers; shard s is bf16 [R][K]
  *   num_shards  S, 1..64
  *   rows_per_shard R >= 1; M = S*R <= max_rows
- *   K           multiple of 64
+ *   K           multiple of 64, at most 32768
  *   W           device, bf16 [K][N]
  *   N           multiple of 256
  *   gathered    device, bf16 [M][K]: receives G[s*R + i] = shard s row i
@@ -118,7 +118,7 @@ long long tovl_dispatch_rows(int T, int k, int E);
  * FIFO-pipeline page; row-block counters with padding seeds of section 5).
  *   x           device, bf16 [T][H]
  *   topk_idx    device, int32 [T][k]: expert of pair (t, j), each in [0, E)
- *   H           multiple of 64 (the GEMM K)
+ *   H           multiple of 64, at most 32768 (the GEMM K)
  *   W           device, bf16 [E][H][N], N multiple of 256
  *   dispatched  device, bf16 [tovl_dispatch_rows(T,k,E)][H]: rows of expert e
  *               occupy [off[e], off[e] + count[e]) in ascending (t, j) order;
@@ -199,6 +199,16 @@ int tovl_get_option(tovl_handle h, int option, long long* value);
  * [1] earliest consumer start ns, [2] latest consumer end ns, [3] earliest
  * producer start ns, [4] latest producer end ns. */
 int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n);
+
+/* Timeline of the last fused call made with statistics on (%globaltimer ns):
+ *   what 0: publish time of each chunk slice [n_chunks], index chunk*k_slices + slice
+ *           (0 where no producer thread published it)
+ *   what 1: time the consumer's gate passed each (tile, slice) [tiles*k_slices]
+ *   what 2: time each tile's output was stored [tiles]
+ * Tiles are numbered row block * (N/256) + column block; for dispatch calls
+ * the tile count is the bound tovl_dispatch_rows/128 * N/256 (unused tiles
+ * read 0).  n must not exceed the stated length. */
+int tovl_read_trace(tovl_handle h, int what, long long* out, long long n);
 
 /* Publish and first-observe %globaltimer stamps of the first n chunks of the
  * last stamped tovl_gated_copy. */
