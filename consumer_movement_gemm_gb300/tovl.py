@@ -86,6 +86,7 @@ SIGNATURES = {
     "tovl_read_stats": ([_P, _ULLP, _I], _I),
     "tovl_read_latency": ([_P, _P, _P, _I], _I),
     "tovl_read_trace": ([_P, _I, _P, _LL], _I),
+    "tovl_dispatch_plan_noalloc": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "tovl_num_sms": ([_P], _I),
     "tovl_error_string": ([_I], ctypes.c_char_p),
     "tovl_last_error": ([_P], ctypes.c_char_p),
@@ -148,6 +149,14 @@ def default_config(device: int = 0) -> tovl_config:
 
 def dispatch_rows(T: int, k: int, E: int) -> int:
     return load().tovl_dispatch_rows(T, k, E)
+
+
+def dispatch_plan_noalloc(topk, E: int, expert_offsets, dst_rows, stream=None) -> None:
+    """Routing plan without allocating (library-owned fixed scratch)."""
+    T, k = topk.shape
+    rc = load().tovl_dispatch_plan_noalloc(_ptr(topk), T, k, E, _ptr(expert_offsets), _ptr(dst_rows),
+                                           _stream(stream))
+    _check(None, rc, "tovl_dispatch_plan_noalloc")
 
 
 class Handle:

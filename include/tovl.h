@@ -135,6 +135,37 @@ int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const
                                const void* W, int N, void* dispatched, int* expert_offsets, void* out,
                                void* stream);
 
+/* ---------------------------------------------------------------- no-allocation plan
+ * The pages have no counterpart to this entry point; it serves callers that
+ * must not allocate device memory themselves (code inside another
+ * framework's memory budget, latency-critical loops that cannot afford
+ * cudaMalloc's device-wide synchronisation, plugins whose host owns every
+ * allocation).
+ *
+ * tovl_dispatch_plan_noalloc computes the routing plan of a dispatch round
+ * -- the same kernels and results as tovl_dispatch_grouped_gemm's plan --
+ * without a handle and without allocating: its scratch is one fixed device
+ * array inside the library (about 0.3 MB, held by every GPU that loads the
+ * library until the process exits).
+ *   topk_idx        device, int32 [T][k], expert of each pair in [0, E)
+ *   expert_offsets  device, int32 [E+1]: padded segment starts (multiples of
+ *                   128); all zero if an expert id is out of range
+ *   dst_rows        device, int32 [T*k]: destination row of each pair, rows
+ *                   of one expert in ascending (t, j) order
+ *   stream          cudaStream_t; the call is asynchronous
+ * Limits: T*k <= TOVL_NOALLOC_MAX_PAIRS and E <= TOVL_NOALLOC_MAX_EXPERTS;
+ * larger sizes return TOVL_ERR_UNSUPPORTED before anything is enqueued.
+ * It runs on the calling thread's current device.  The first call on a
+ * device looks up the scratch array's device address (cudaGetSymbolAddress)
+ * and keeps it; make that first call before any stream capture.  All calls
+ * on a device share the one array and it keeps the previous call's
+ * contents, so calls whose kernels overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller. */
+#define TOVL_NOALLOC_MAX_PAIRS 32768
+#define TOVL_NOALLOC_MAX_EXPERTS 64
+int tovl_dispatch_plan_noalloc(const int* topk_idx, int T, int k, int E, int* expert_offsets, int* dst_rows,
+                               void* stream);
+
 /* ---------------------------------------------------------------- controls
  * The acceptance method of the platform page, section 5, compares the fused
  * kernel with its parts run alone on the same SM counts. */
