@@ -1,0 +1,43 @@
+// common.cuh -- helpers shared by the producer and consumer roles of the
+// fused kernel.
+#pragma once
+#include "ctrl.cuh"
+#include "ptx.cuh"
+
+namespace tovl {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return reinterpret_cast<uint8_t*>((a + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ void stat_min(const FusedParams& p, int idx, unsigned long long v)
+{
+    if (p.stats) atomicMin(p.ctrl.stats + idx, v);
+}
+
+__device__ __forceinline__ void stat_max(const FusedParams& p, int idx, unsigned long long v)
+{
+    if (p.stats) atomicMax(p.ctrl.stats + idx, v);
+}
+
+__device__ __forceinline__ void trace_put(const FusedParams& p, long long idx, unsigned long long v)
+{
+    if (p.stats && idx < p.ctrl.trace_cap) p.ctrl.trace[idx] = static_cast<long long>(v);
+}
+
+// Number of 128-row blocks the producers fill and the consumers traverse.
+__device__ __forceinline__ int num_row_blocks(const FusedParams& p)
+{
+    if (p.mode == kModeGather) return (p.M + kTileM - 1) / kTileM;
+    return p.meta[1];
+}
+
+// K-blocks [kb_begin(s), kb_begin(s+1)) form slice s.
+__device__ __forceinline__ int kb_begin(const FusedParams& p, int s)
+{
+    return s * p.n_kb / p.k_slices;
+}
+
+}  // namespace tovl

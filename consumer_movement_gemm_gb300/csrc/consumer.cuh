@@ -1,0 +1,368 @@
+// consumer.cuh -- consumer CTAs of the fused kernel: gated tcgen05 GEMM.
+//
+// A consumer CTA (or a pair of CTAs in a cluster, PAIR = 2) computes output
+// tiles in row-block order, the producers' order ("cross-GPU sync protocols
+// on PCIe", section 6 item 3).  Warp roles:
+//   warp 0      TMA: per tile and K-slice, waits for the slice's gate, then
+//               streams A (gathered rows) and B (weights) k-blocks into a
+//               ring of shared-memory stages
+//   warp 1      MMA: one lane issues tcgen05.mma into a double-buffered TMEM
+//               accumulator (2 x 256 fp32 columns)
+//   warps 2-9   epilogue: TMEM -> registers -> bf16 (nearest even) -> out
+//   warp 10     gate: polls the protocol (acquire loads of local slots /
+//               counters, ballot) ahead of the TMA warp and hands each
+//               passed gate over through shared memory
+// PAIR = 1: 128x256 tiles, stage = A 16 KB + B 32 KB, 4 stages.
+// PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
+// own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 6 stages); the
+// pair's first CTA issues the MMAs, which read A and B halves from both CTAs
+// and accumulate each CTA's rows in its own TMEM.  Both CTAs' TMA loads are
+// counted on the first CTA's "full" barriers; MMA completion is multicast to
+// both CTAs; each CTA's epilogue warps release the accumulator on the first
+// CTA's "tmem empty" barrier.
+#pragma once
+#include "common.cuh"
+#include "ctrl.cuh"
+#include "ptx.cuh"
+#include "sync.cuh"
+
+namespace tovl {
+
+template <int PAIR>
+struct Tile {
+    static constexpr int kStages = PAIR == 1 ? 4 : 6;
+    static constexpr int kStageA = kTileM * kTileK * 2;               // 16 KB
+    static constexpr int kStageB = kTileK * kTileN * 2 / PAIR;        // this CTA's B columns
+    static constexpr int kStageBytes = kStageA + kStageB;
+    static constexpr int kBBoxes = kTileN / 64 / PAIR;                // 64-column TMA boxes per stage
+    // M = 128 * PAIR, N = 256, A K-major, B MN-major (W is [K][N], N contiguous)
+    static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM * PAIR, kTileN, false, true);
+    static_assert(kStages * kStageBytes + 1024 <= kSmemBytes, "stages must fit the dynamic shared memory");
+};
+
+template <int PAIR>
+struct ConsumerSmem {
+    uint8_t* a;          // kStages x [128 rows][128 B]  (A tile, 128B swizzle)
+    uint8_t* b;          // kStages x kBBoxes x [64 k-rows][128 B]  (this CTA's B columns)
+    uint64_t* full;      // TMA -> MMA (in the pair's first CTA: counts both CTAs' bytes)
+    uint64_t* empty;     // MMA -> TMA
+    uint64_t* tfull;     // MMA -> epilogue (per accumulator)
+    uint64_t* tempty;    // epilogue -> MMA (in the pair's first CTA: both CTAs' warps)
+    uint32_t* tmem_slot;
+    int* gates_passed;   // gate warp -> TMA warp: number of (tile, slice) gates passed
+};
+
+template <int PAIR>
+__device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
+{
+    using T = Tile<PAIR>;
+    ConsumerSmem<PAIR> s;
+    s.a = smem;
+    s.b = smem + T::kStages * T::kStageA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kStages * T::kStageBytes);
+    s.full = bars;
+    s.empty = bars + T::kStages;
+    s.tfull = bars + 2 * T::kStages;
+    s.tempty = bars + 2 * T::kStages + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * T::kStages + 4);
+    s.gates_passed = reinterpret_cast<int*>(bars + 2 * T::kStages + 5);
+    return s;
+}
+
+// Tiles of this consumer unit (a CTA, or a CTA pair): unit u of n_units
+// takes tiles u, u + n_units, ...; a tile covers PAIR consecutive row blocks
+// and one 256-column block.
+template <int PAIR>
+struct Schedule {
+    int unit, n_units, n_tiles;
+    uint32_t rank;
+    __device__ int row_block(const FusedParams& p, int t) const { return (t / p.n_nb) * PAIR + static_cast<int>(rank); }
+};
+
+template <int PAIR>
+__device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, int cid)
+{
+    Schedule<PAIR> sc;
+    sc.rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
+    sc.unit = cid / PAIR;
+    sc.n_units = p.n_consumers / PAIR;
+    sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb;
+    return sc;
+}
+
+// Gate: the rows of row block mb, K-slice s, are complete this round.
+__device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb, int s)
+{
+    const int* words[kTileM / kChunkRows];
+    int n = 0;
+    int target;
+    const int S = p.ctrl.n_slices;
+    if (p.mode == kModeGather) {
+        const int c0 = mb * (kTileM / kChunkRows);
+        for (int i = 0; i < kTileM / kChunkRows; ++i)
+            if ((c0 + i) * kChunkRows < p.M) words[n++] = p.ctrl.slot + (c0 + i) * S + s;
+        target = p.gate_seq;
+    } else {
+        words[n++] = p.ctrl.rbcnt + mb * S + s;
+        target = p.gate_seq * kBlockRows;
+    }
+    const int r = warp_wait_ge(words, n, target, p.ctrl, p.seq, p.timeout_ns);
+    return static_cast<unsigned long long>(r < 0 ? -r : r);
+}
+
+// Gate warp: walks this CTA's (tile, slice) schedule ahead of the TMA warp,
+// waits for each slice's rows on the protocol and hands every passed gate to
+// the TMA warp with a CTA-scope release of the running count.  A gate that
+// times out is handed on as well, so the pipeline drains; the status word
+// holds the error.
+template <int PAIR>
+__device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
+{
+    const uint32_t lane = ptx::lane_id();
+    unsigned long long polls = 0;
+    int passed = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
+        const int mb = sc.row_block(p, t);
+        for (int sl = 0; sl < p.k_slices; ++sl) {
+            polls += gate(p, mb, sl);
+            ++passed;
+            if (lane == 0) {
+                ptx::st_release_cta_smem(s.gates_passed, passed);
+                trace_put(p, static_cast<long long>(t) * p.k_slices + sl, ptx::globaltimer());
+            }
+            __syncwarp();
+        }
+    }
+    if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
+}
+
+// TMA lane: wait until the gate warp has passed gate number `idx` (bounded).
+template <int PAIR>
+__device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, int idx)
+{
+    if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+            record_error(p.ctrl, kErrTimeout);
+            return false;
+        }
+        __nanosleep(20);
+    }
+}
+
+// TMA warp: per tile and K-slice, wait for the slice's gate, then stream A
+// and B k-blocks into the stage ring.  One lane issues everything.
+template <int PAIR>
+__device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
+{
+    using T = Tile<PAIR>;
+    if (ptx::lane_id() != 0) return;
+    uint32_t stage = 0, phase = 0;
+    int gate_idx = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
+        const int mb = sc.row_block(p, t);
+        const int nb = t % p.n_nb;
+        const int brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
+        const int n0 = nb * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+        for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
+            if (p.gated) {
+                if (!wait_gate(p, s, gate_idx)) return;
+                // the rows were written through the generic proxy; order them
+                // before this thread's tensor-memory-access (async proxy) reads
+                ptx::fence_proxy_async_global();
+            }
+            const int kb1 = kb_begin(p, sl + 1);
+            for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
+                if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
+                uint8_t* adst = s.a + stage * T::kStageA;
+                uint8_t* bdst = s.b + stage * T::kStageB;
+                if (PAIR == 1) {
+                    ptx::mbar_arrive_expect_tx(&s.full[stage], T::kStageBytes);
+                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
+#pragma unroll
+                    for (int j = 0; j < T::kBBoxes; ++j)
+                        ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[stage], n0 + j * 64,
+                                         brow + kb * kTileK);
+                } else {
+                    // both CTAs' bytes are counted on the first CTA's barrier
+                    if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[stage], PAIR * T::kStageBytes);
+                    const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
+                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, mb * kTileM);
+#pragma unroll
+                    for (int j = 0; j < T::kBBoxes; ++j)
+                        ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, n0 + j * 64,
+                                              brow + kb * kTileK);
+                }
+                if (++stage == T::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+}
+
+// MMA warp: one lane (of the pair's first CTA) issues the MMAs.
+template <int PAIR>
+__device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                             uint32_t tmem_base)
+{
+    using T = Tile<PAIR>;
+    if (ptx::lane_id() != 0 || sc.rank != 0) return;
+    uint32_t stage = 0, phase = 0;
+    int local = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
+        const uint32_t acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + acc * kTileN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+            if (!mbar_wait(&s.full[stage], phase, p.ctrl, p.pipe_timeout_ns)) return;
+            ptx::tc_fence_after();
+            const uint32_t a0 = ptx::smem_u32(s.a + stage * T::kStageA);
+            const uint32_t b0 = ptx::smem_u32(s.b + stage * T::kStageB);
+#pragma unroll
+            for (int k = 0; k < kTileK / kUmmaK; ++k) {
+                // A: K-major, 128B swizzle; +32 B per 16-element k step inside
+                //    the swizzle row; 8-row groups 1024 B apart.
+                const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
+                // B: MN-major, 128B swizzle; +2048 B per 16 k-rows; 8-k-row
+                //    groups 1024 B apart; 64-column blocks 8 KB apart.
+                const uint64_t bd = ptx::smem_desc_sw128(b0 + k * 2048, kTileK * 128, 1024);
+                if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                else ptx::umma_bf16_pair(d, ad, bd, T::kIdesc, (kb | k) != 0);
+            }
+            if (PAIR == 1) ptx::umma_commit(&s.empty[stage]);
+            else ptx::umma_commit_pair(&s.empty[stage], 0x3);
+            if (++stage == T::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (PAIR == 1) ptx::umma_commit(&s.tfull[acc]);
+        else ptx::umma_commit_pair(&s.tfull[acc], 0x3);
+    }
+}
+
+// Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) -> out.
+// Warp w reads TMEM lane quarter w % 4 (the quarter its position allows) and
+// one half of the 256 accumulator columns.
+template <int PAIR>
+__device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                  uint32_t tmem_base, int valid_rows)
+{
+    const int warp = threadIdx.x / 32;
+    const uint32_t lane = ptx::lane_id();
+    const int q = warp & 3;
+    const int half = (warp - kEpiWarp0) / 4;
+    const int row_in_tile = q * 32 + static_cast<int>(lane);
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    int local = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
+        const int mb = sc.row_block(p, t);
+        const int nb = t % p.n_nb;
+        const uint32_t acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
+        if (!__all_sync(0xffffffffu, arrived)) return;
+        ptx::tc_fence_after();
+        const int row = mb * kTileM + row_in_tile;
+        const bool ok = row < valid_rows;
+        const int col0 = half * (kTileN / 2);
+        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + nb * kTileN + col0);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + col0;
+#pragma unroll 1
+        for (int c = 0; c < kTileN / 2 / 32; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+            ptx::tmem_ld_wait();
+            if (ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                    w.y = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                    w.z = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                    w.w = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                    dst[c * 4 + v] = w;
+                }
+            }
+        }
+        // this warp's reads of the accumulator are done: one arrival per warp
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (PAIR == 1) ptx::mbar_arrive(&s.tempty[acc]);
+            else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
+            if (p.stats) {
+                const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
+                if (idx < p.ctrl.trace_cap)
+                    atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+            }
+        }
+    }
+}
+
+template <int PAIR>
+__device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
+{
+    using T = Tile<PAIR>;
+    const int warp = threadIdx.x / 32;
+    const ConsumerSmem<PAIR> s = consumer_smem<PAIR>(smem);
+    const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < T::kStages; ++i) {
+            ptx::mbar_init(&s.full[i], 1);
+            ptx::mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&s.tfull[i], 1);
+            ptx::mbar_init(&s.tempty[i], kEpiWarps * PAIR);
+        }
+        *s.gates_passed = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&p.tmap_a);
+        ptx::prefetch_tmap(&p.tmap_b);
+        stat_min(p, kStatConsStartNs, ptx::globaltimer());
+    }
+    if (warp == 1) {
+        if (PAIR == 1) {
+            ptx::tmem_alloc(s.tmem_slot, kTmemCols);
+            ptx::tmem_relinquish();
+        } else {
+            ptx::tmem_alloc_pair(s.tmem_slot, kTmemCols);
+            ptx::tmem_relinquish_pair();
+        }
+    }
+    ptx::tc_fence_before();
+    // barriers initialised and TMEM allocated in both CTAs before any
+    // cross-CTA arrival or load
+    if (PAIR == 1) __syncthreads();
+    else ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_slot;
+
+    const int valid_rows = (p.mode == kModeGather) ? p.M : p.meta[0];
+    if (warp == 0) consumer_tma<PAIR>(p, s, sc);
+    else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
+    else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base, valid_rows);
+    else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
+    __syncwarp();
+
+    // teardown: every role of both CTAs has finished before TMEM is freed
+    // (and before a CTA whose shared memory the peer reads exits)
+    ptx::tc_fence_before();
+    if (PAIR == 1) __syncthreads();
+    else ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        if (PAIR == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+        else ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+    if (threadIdx.x == 0) stat_max(p, kStatConsEndNs, ptx::globaltimer());
+}
+
+}  // namespace tovl

@@ -26,7 +26,6 @@ constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
 constexpr int kTraceCap = 1 << 20; // timeline entries kept when statistics are on
 constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
 constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)
-constexpr int kReleaseBatch = 4;   // producer items per batched release
 constexpr int kMaxShards = 64;
 constexpr int kMaxK = 32768;       // a producer ring stage must hold one 64 KB row
 constexpr int kMaxExperts = 512;

@@ -5,9 +5,10 @@
 
 namespace tovl {
 
-cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative);
+cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair);
 cudaError_t prepare_fused();
 int fused_max_active_per_sm();
+int fused_max_active_pairs();
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t prepare_plan();

@@ -37,6 +37,9 @@ struct tovl_ctx {
     int copy_waiters = 0;    // copy sweep waiters (0 = auto)
     int fault_gate_offset = 0;  // test hook: gates wait for seq + offset
     int slices = 1;          // K-slices per chunk watermark (fixed per handle)
+    int pair_mode = 1;       // gather calls use CTA-pair (cta_group::2) consumers when possible
+    int max_pairs = 0;       // co-resident CTA pairs of the pair kernel on this device
+    bool coop_pairs = true;  // cooperative launch accepted together with clusters
     long long seq = 0;
     Ctrl ctrl{};
     Plan plan{};
@@ -213,6 +216,7 @@ TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
         if ((e = prepare_plan()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare plan"); break; }
         if ((e = prepare_copy()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare copy"); break; }
         if (fused_max_active_per_sm() < 1) { rc = TOVL_ERR_UNSUPPORTED; break; }
+        h->max_pairs = fused_max_active_pairs();
 
         const int n_chunks = static_cast<int>(ceil_div(cfg.max_rows, kChunkRows));
         const int n_blocks = static_cast<int>(ceil_div(cfg.max_rows, kBlockRows));
@@ -318,34 +322,57 @@ static void base_params(tovl_ctx* h, FusedParams& p)
 // 10 TFLOP/s per consumer SM), then grows while the consumers still finish
 // the tiles in the same number of waves (section 4 of the platform page: SMs
 // given to communication are taken from the GEMM, so the split is swept).
-static void split_ctas(tovl_ctx* h, int& P, int& C, long long tiles, double copy_bytes, double flops)
+// With CTA pairs (pair = 2) a consumer unit is two CTAs computing 256-row
+// tiles, both counts are even, and the grid is limited to the pairs that can
+// be co-resident.
+static void split_ctas(tovl_ctx* h, int& P, int& C, int n_mb, int n_nb, double copy_bytes, double flops, int pair)
 {
-    const int S = h->num_sms;
+    int S = h->num_sms;
+    if (pair == 2 && 2 * h->max_pairs < S) S = 2 * h->max_pairs;
+    const long long tiles = static_cast<long long>((n_mb + pair - 1) / pair) * n_nb;   // per consumer unit
     if (h->producers > 0) {
-        P = h->producers < S - 1 ? h->producers : S - 1;
+        P = h->producers < S - pair ? h->producers : S - pair;
     } else {
         const double tc = copy_bytes / 60e9, tg = flops / 10e12;
         int p = static_cast<int>(S * tc / (tc + tg + 1e-30) + 0.5);
         const int pmax = S / 4;
         p = p < 4 ? 4 : (p > pmax ? pmax : p);
         if (tiles > 0) {
-            const long long waves = (tiles + (S - p) - 1) / (S - p);
-            const int cmin = static_cast<int>((tiles + waves - 1) / waves);
+            const int units = (S - p) / pair;
+            const long long waves = (tiles + units - 1) / units;
+            const int cmin = static_cast<int>((tiles + waves - 1) / waves) * pair;
             if (S - cmin > p) p = S - cmin < pmax ? S - cmin : pmax;
         }
         P = p;
     }
+    if (pair == 2) P = (P + 1) & ~1;
     C = h->consumers ? h->consumers : S - P;
     if (C > S - P) C = S - P;
-    if (C < 1) C = 1;
+    if (pair == 2) C &= ~1;
+    if (C < pair) C = pair;
     h->last_P = P;
     h->last_C = C;
+}
+
+// Launch with the cooperative guarantee of co-residency; a device that does
+// not accept it together with a cluster shape is launched without it (the
+// grid still fits: one CTA per SM, at most the co-resident pairs).
+static cudaError_t launch(tovl_ctx* h, const FusedParams& p, cudaStream_t s, bool cooperative, int pair)
+{
+    if (pair == 2 && !h->coop_pairs) cooperative = false;
+    cudaError_t e = launch_fused(p, s, cooperative, pair);
+    if (e != cudaSuccess && pair == 2 && cooperative) {
+        cudaGetLastError();
+        e = launch_fused(p, s, false, pair);
+        if (e == cudaSuccess) h->coop_pairs = false;
+    }
+    return e;
 }
 
 // Slicing and producer-item geometry of one call: k_slices never exceeds the
 // K-blocks; an item moves item_rows rows of one slice, at most 8 KB per pass;
 // the producers' ordering group is the consumers' first wave of row blocks.
-static void call_geometry(const tovl_ctx* h, FusedParams& p, int C)
+static void call_geometry(const tovl_ctx* h, FusedParams& p, int C, int pair)
 {
     p.k_slices = h->slices < p.n_kb ? h->slices : p.n_kb;
     const int max_kbs = (p.n_kb + p.k_slices - 1) / p.k_slices;
@@ -353,7 +380,8 @@ static void call_geometry(const tovl_ctx* h, FusedParams& p, int C)
     int ri = 64;
     while (ri > 1 && ri * n16 > kItemInt4) ri >>= 1;
     p.item_rows = ri;
-    p.wave_blocks = C > 0 ? (C + p.n_nb - 1) / p.n_nb : 1;
+    const int units = C / pair;
+    p.wave_blocks = units > 0 ? (units + p.n_nb - 1) / p.n_nb * pair : 1;
     if (p.wave_blocks < 1) p.wave_blocks = 1;
 }
 
@@ -410,13 +438,17 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     p.n_kb = K / kTileK;
     p.n_nb = N / kTileN;
     p.row_bytes = K * 2;
+    // the split (and with it P for copy-only and C for GEMM-only) is the one
+    // the fused call uses; only launches with consumers need CTA pairs
+    const int split_pair = (h->pair_mode && h->max_pairs > 0) ? 2 : 1;
+    const int pair = (flags & 2) ? split_pair : 1;
+    const int n_mb = (M + kTileM - 1) / kTileM;
     int P, C;
-    split_ctas(h, P, C, static_cast<long long>((M + kTileM - 1) / kTileM) * p.n_nb, 4.0 * M * K,
-               2.0 * M * static_cast<double>(N) * K);
+    split_ctas(h, P, C, n_mb, p.n_nb, 4.0 * M * K, 2.0 * M * static_cast<double>(N) * K, split_pair);
     p.n_producers = (flags & 1) ? P : 0;
     p.n_consumers = (flags & 2) ? C : 0;
     p.gated = (flags & 4) ? 1 : 0;
-    call_geometry(h, p, C);
+    call_geometry(h, p, C, split_pair);
     p.n_shards = S;
     p.rows_per_shard = R;
     for (int s = 0; s < S; ++s) p.shard[s] = shards ? shards[s] : nullptr;
@@ -432,9 +464,9 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     if (round) p.seq = static_cast<int>(h->seq + 1);
     else p.seq = static_cast<int>(h->seq);
     p.gate_seq = p.seq + h->fault_gate_offset;
-    p.trace_tiles = (flags & 2) ? ((M + kTileM - 1) / kTileM) * p.n_nb : 0;
+    p.trace_tiles = (flags & 2) ? (n_mb + pair - 1) / pair * p.n_nb : 0;
     if ((rc = reset_stats(h, stream, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
-    const cudaError_t e = launch_fused(p, stream, (flags & 4) != 0);
+    const cudaError_t e = launch(h, p, stream, (flags & 4) != 0, pair);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
     if (round) h->seq += 1;
     h->last_stream = stream;
@@ -522,11 +554,12 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.n_nb = N / kTileN;
     p.row_bytes = H * 2;
     int P, C;
-    split_ctas(h, P, C, rows / kTileM * p.n_nb, 4.0 * pairs * H, 2.0 * pairs * static_cast<double>(N) * H);
+    split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
+               2.0 * pairs * static_cast<double>(N) * H, 1);
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 1;
-    call_geometry(h, p, C);
+    call_geometry(h, p, C, 1);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;
     p.pad = h->plan.pad;
@@ -545,7 +578,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.gate_seq = p.seq + h->fault_gate_offset;
     p.trace_tiles = static_cast<int>(rows / kTileM * p.n_nb);
     if ((rc = reset_stats(h, s, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
-    e = launch_fused(p, s, true);
+    e = launch(h, p, s, true, 1);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
     h->seq += 1;
     h->last_stream = s;
@@ -750,6 +783,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value < 0 || value > 1000) return TOVL_ERR_INVALID;
         h->fault_gate_offset = static_cast<int>(value);
         return TOVL_OK;
+    case 10:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->pair_mode = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -768,6 +805,9 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 6: *value = h->copy_ctas; return TOVL_OK;
     case 7: *value = h->copy_waiters; return TOVL_OK;
     case 8: *value = h->fault_gate_offset; return TOVL_OK;
+    case 10: *value = (h->pair_mode && h->max_pairs > 0) ? 1 : 0; return TOVL_OK;
+    case 11: *value = h->max_pairs; return TOVL_OK;
+    case 12: *value = h->coop_pairs ? 1 : 0; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

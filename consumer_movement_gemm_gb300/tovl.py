@@ -33,6 +33,9 @@ OPT_COPY_CTAS = 6
 OPT_COPY_WAITERS = 7
 OPT_FAULT_GATE_OFFSET = 8
 OPT_K_SLICES = 9
+OPT_PAIRS = 10
+OPT_MAX_PAIRS = 11
+OPT_COOP_PAIRS = 12
 
 
 class TovlError(RuntimeError):

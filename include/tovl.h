@@ -219,6 +219,11 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
 /* Options for sweeps: 1 = producer CTAs, 2 = consumer CTAs, 3 = copy mode,
  * 4 = statistics on/off, 5 = wait timeout in ns, 6 = copy-sweep CTAs,
  * 7 = copy-sweep waiter CTAs, 9 = k_slices (read only),
+ * 10 = CTA-pair consumers for gather calls (1 = on, the default: two CTAs of a
+ * cluster compute a 256x256 tile with cta_group::2 MMAs; 0 = one CTA per
+ * 128x256 tile; reads back 0 if the device cannot co-schedule pairs),
+ * 11 = co-resident CTA pairs on the device (read only), 12 = 1 if
+ * cooperative launches are accepted with pairs (read only),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

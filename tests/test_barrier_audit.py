@@ -3,9 +3,10 @@
 The sync-protocol page (section 6, item 4) warns that __syncthreads() is
 hardware barrier 0 counting the whole CTA; if role-specialised warps use the
 same id with another thread count, the result is undefined.  The kernels here
-use barrier 0 only at full-CTA points -- before the role split and at
-teardown -- and no named barriers at all; warp roles coordinate through
-mbarriers.  This test pins that map."""
+use barrier 0 (or, for CTA pairs, the cluster barrier) only at full-CTA
+points -- before the role split and at teardown -- and no named barriers at
+all; warp roles coordinate through mbarriers and a shared-memory hand-off.
+This test pins that map."""
 import os
 import re
 
@@ -14,12 +15,14 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 # functions that run after the role split: no CTA-wide barrier may appear
 ROLE_FUNCTIONS = {
-    "fused.cu": ["consumer_tma", "consumer_mma", "consumer_epilogue", "gate", "seed_counters", "copy_item"],
+    "consumer.cuh": ["consumer_tma", "consumer_mma", "consumer_epilogue", "gate", "consumer_gate", "wait_gate"],
+    "producer.cuh": ["seed_counters", "copy_item"],
     "copyplane.cuh": ["bulk_stream", "run_bulk"],
     "copy.cu": ["copy_v4", "copy_waiter", "copy_seeds"],
 }
-# full-CTA barrier-0 sites allowed per function
-ALLOWED_SYNCTHREADS = {("fused.cu", "consumer"): 2, ("fused.cu", "producer"): 1}
+# full-CTA barrier sites allowed per function: (file, function) -> count
+ALLOWED_SYNCTHREADS = {("consumer.cuh", "consumer"): 2, ("producer.cuh", "producer"): 1}
+ALLOWED_CLUSTER_SYNC = {("consumer.cuh", "consumer"): 2}
 
 
 def _function_body(src: str, name: str) -> str:
@@ -36,7 +39,8 @@ def _function_body(src: str, name: str) -> str:
 def test_no_named_barriers():
     for f in os.listdir(CSRC):
         text = open(os.path.join(CSRC, f)).read()
-        assert not re.search(r"\bbar(rier)?\.(sync|arrive|red)\b", text), f
+        assert not re.search(r"\bbar\.(sync|arrive|red)\b", text), f
+        assert not re.search(r"\bbarrier\.(sync|arrive|red)\b", text), f
         assert "named_barrier" not in text, f
 
 
@@ -44,17 +48,24 @@ def test_no_cta_barrier_inside_roles():
     for f, names in ROLE_FUNCTIONS.items():
         text = open(os.path.join(CSRC, f)).read()
         for n in names:
-            assert "__syncthreads" not in _function_body(text, n), (f, n)
+            body = _function_body(text, n)
+            assert "__syncthreads" not in body, (f, n)
+            assert "cluster_sync" not in body, (f, n)
 
 
 def test_cta_barrier_sites_are_the_audited_ones():
-    text = open(os.path.join(CSRC, "fused.cu")).read()
     for (f, n), count in ALLOWED_SYNCTHREADS.items():
         body = _function_body(open(os.path.join(CSRC, f)).read(), n)
         assert body.count("__syncthreads()") == count, (f, n)
-    # every CTA barrier in the consumer is preceded by a warp reconvergence or
-    # sits before the role split
-    body = _function_body(text, "consumer")
-    split = body.index("consumer_tma(")
-    tail = body[split:]
+    for (f, n), count in ALLOWED_CLUSTER_SYNC.items():
+        body = _function_body(open(os.path.join(CSRC, f)).read(), n)
+        assert body.count("cluster_sync()") == count, (f, n)
+    # every CTA barrier after the role split is preceded by a warp reconvergence
+    body = _function_body(open(os.path.join(CSRC, "consumer.cuh")).read(), "consumer")
+    tail = body[body.index("consumer_tma<"):]
     assert tail.index("__syncwarp()") < tail.index("__syncthreads()")
+    # the only cluster barrier instructions live in the one helper
+    for f in os.listdir(CSRC):
+        text = open(os.path.join(CSRC, f)).read()
+        if "barrier.cluster" in text:
+            assert f == "ptx.cuh", f

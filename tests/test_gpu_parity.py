@@ -46,8 +46,10 @@ def _check_ctrl(h, R):
 
 # ------------------------------------------------------------------ GEMM alone
 @pytest.mark.parametrize("M,K,N", [(256, 256, 256), (128, 512, 512)])
-def test_gemm_only_identity_is_exact(M, K, N):
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gemm_only_identity_is_exact(M, K, N, pairs):
     with _handle() as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
         A = workloads.bf16_normal((M, K), 1.0, 11, DEV)
         W = torch.zeros(K, N, dtype=torch.bfloat16, device=DEV)
         idx = torch.arange(min(K, N), device=DEV)
@@ -60,9 +62,11 @@ def test_gemm_only_identity_is_exact(M, K, N):
         assert torch.equal(out, want)
 
 
-@pytest.mark.parametrize("M,K,N", [(384, 320, 512), (300, 192, 256), (1, 64, 256)])
-def test_gemm_only_matches_oracle(M, K, N):
+@pytest.mark.parametrize("M,K,N", [(384, 320, 512), (300, 192, 256), (1, 64, 256), (640, 1024, 768)])
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gemm_only_matches_oracle(M, K, N, pairs):
     with _handle() as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
         A = workloads.bf16_normal((M, K), 1 / math.sqrt(K), 12, DEV)
         W = workloads.bf16_normal((K, N), 1 / math.sqrt(K), 13, DEV)
         out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
@@ -81,9 +85,13 @@ def _gather_round(h, cfg, seed):
 
 
 @pytest.mark.parametrize("k_slices", [1, 2, 4, 8])
-def test_tiny_gather_gemm_three_rounds(k_slices):
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_tiny_gather_gemm_three_rounds(k_slices, pairs):
     cfg = workloads.TINY
     with _handle(k_slices=k_slices) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
+        if pairs:
+            assert h.get_option(tovl.OPT_PAIRS) == 1, "CTA pairs unavailable on this device"
         for r in range(1, cfg.rounds + 1):
             X, W, gathered, out = _gather_round(h, cfg, workloads.round_seed(cfg.seed, r))
             assert h.sync_status() == 0
@@ -96,9 +104,11 @@ def test_tiny_gather_gemm_three_rounds(k_slices):
 
 @pytest.mark.parametrize("S,R,K,N,P,KS", [(3, 100, 192, 256, 4, 2), (1, 64, 64, 512, 1, 4), (5, 77, 128, 256, 32, 1),
                                           (2, 200, 320, 256, 8, 4), (7, 33, 448, 512, 3, 8)])
-def test_gather_gemm_ragged(S, R, K, N, P, KS):
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gather_gemm_ragged(S, R, K, N, P, KS, pairs):
     cfg = workloads.GatherCfg("ragged", S, R, K, N, rounds=2)
     with _handle(producer_ctas=P, k_slices=KS) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
         for r in range(1, 3):
             X, W, gathered, out = _gather_round(h, cfg, 100 + r)
             assert h.sync_status() == 0
@@ -121,9 +131,11 @@ def test_copy_only_control(k_slices):
             _check_ctrl(h, r)
 
 
-def test_timeout_is_reported_and_handle_recovers():
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_timeout_is_reported_and_handle_recovers(pairs):
     cfg = workloads.TINY
     with _handle(wait_timeout_ns=5_000_000, k_slices=2) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
         h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # gates wait for a sequence nobody publishes
         _gather_round(h, cfg, 1)
         assert h.sync_status() == tovl.TOVL_ERR_TIMEOUT
