@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", choices=["fused", "gemm", "copy", "dispatch"], default=None,
                     help="run only W + K calls of one kernel on a small case (for ncu captures) and exit")
+    ap.add_argument("--no-coop", action="store_true",
+                    help="launch fused kernels without the cooperative attribute (profiler replay)")
     return ap.parse_args(argv)
 
 
@@ -127,9 +129,21 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def recorded_traffic(profile: str, source: str):
+FUSED_SOURCES = ["ctrl.cuh", "ptx.cuh", "sync.cuh", "common.cuh", "producer.cuh", "consumer.cuh", "fused.cu"]
+
+
+def kernel_source_sha(files=FUSED_SOURCES) -> str:
+    """sha256 over the fused kernel's sources, in a fixed order."""
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "consumer_movement_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(profile: str):
     """DRAM bytes per launch from an ncu summary under profiles/, if it was
-    taken on the current kernel source (its sha256 is recorded there)."""
+    taken on the current kernel sources (their sha256 is recorded there)."""
     path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
@@ -138,8 +152,7 @@ def recorded_traffic(profile: str, source: str):
     m_b = re.search(r"dram-bytes-per-launch:\s*([0-9.eE+]+)", text)
     if not m_sha or not m_b:
         return None
-    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()
-    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+    return float(m_b.group(1)) if kernel_source_sha() == m_sha.group(1) else None
 
 
 def dist_init(args):
@@ -476,7 +489,7 @@ def run_tovl(args):
         return
     tf = cfg.flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    traffic = recorded_traffic("fused_gather_gemm_tp.md", "consumer_movement_gemm_gb300/csrc/fused.cu")
+    traffic = recorded_traffic("fused_gather_gemm_tp.md")
     cpu = cpu_oracle_sample(cfg, args.cpu_seconds)
     cpu.pop("seconds", None)
     line = {
@@ -522,6 +535,8 @@ def run_profile(args):
     if args.profile in ("fused", "gemm"):
         cfg = workloads.TP
         with tovl.Handle(0, max_rows=1 << 14, producer_ctas=args.producers, k_slices=args.k_slices) as h:
+            if args.no_coop:
+                h.set_option(tovl.OPT_COOPERATIVE, 0)
             X, W, gathered, out = tp_setup(h, cfg, dev)
             for _ in range(n):
                 if args.profile == "fused":
@@ -543,6 +558,8 @@ def run_profile(args):
         x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
         rows = tovl.dispatch_rows(cfg.T, cfg.k, cfg.E)
         with tovl.Handle(0, max_rows=rows, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=args.k_slices) as h:
+            if args.no_coop:
+                h.set_option(tovl.OPT_COOPERATIVE, 0)
             topk = torch.from_numpy(topk_np).to(dev)
             dispatched = torch.zeros(rows, cfg.H, dtype=torch.bfloat16, device=dev)
             offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)

@@ -40,6 +40,7 @@ struct tovl_ctx {
     int pair_mode = 1;       // gather calls use CTA-pair (cta_group::2) consumers when possible
     int max_pairs = 0;       // co-resident CTA pairs of the pair kernel on this device
     bool coop_pairs = true;  // cooperative launch accepted together with clusters
+    bool coop_enabled = true;  // fused launches ask for the co-residency guarantee
     long long seq = 0;
     Ctrl ctrl{};
     Plan plan{};
@@ -360,6 +361,7 @@ static void split_ctas(tovl_ctx* h, int& P, int& C, int n_mb, int n_nb, double c
 static cudaError_t launch(tovl_ctx* h, const FusedParams& p, cudaStream_t s, bool cooperative, int pair)
 {
     if (pair == 2 && !h->coop_pairs) cooperative = false;
+    if (!h->coop_enabled) cooperative = false;
     cudaError_t e = launch_fused(p, s, cooperative, pair);
     if (e != cudaSuccess && pair == 2 && cooperative) {
         cudaGetLastError();
@@ -787,6 +789,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != 0 && value != 1) return TOVL_ERR_INVALID;
         h->pair_mode = static_cast<int>(value);
         return TOVL_OK;
+    case 13:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->coop_enabled = value != 0;
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -808,6 +814,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 10: *value = (h->pair_mode && h->max_pairs > 0) ? 1 : 0; return TOVL_OK;
     case 11: *value = h->max_pairs; return TOVL_OK;
     case 12: *value = h->coop_pairs ? 1 : 0; return TOVL_OK;
+    case 13: *value = h->coop_enabled ? 1 : 0; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

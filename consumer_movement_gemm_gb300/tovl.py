@@ -36,6 +36,7 @@ OPT_K_SLICES = 9
 OPT_PAIRS = 10
 OPT_MAX_PAIRS = 11
 OPT_COOP_PAIRS = 12
+OPT_COOPERATIVE = 13
 
 
 class TovlError(RuntimeError):

@@ -223,7 +223,10 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * cluster compute a 256x256 tile with cta_group::2 MMAs; 0 = one CTA per
  * 128x256 tile; reads back 0 if the device cannot co-schedule pairs),
  * 11 = co-resident CTA pairs on the device (read only), 12 = 1 if
- * cooperative launches are accepted with pairs (read only),
+ * cooperative launches are accepted with pairs (read only), 13 = fused
+ * launches request the cooperative co-residency guarantee (1, the default;
+ * 0 launches the same kernel without it, for tools that cannot replay
+ * cooperative launches -- the grid still fits one CTA per SM),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in
