@@ -298,13 +298,20 @@ def tp_setup(h, cfg, dev):
     return X, W, gathered, out
 
 
-def acceptance(h, timer, cfg, X, W, gathered, out, n: int):
+def acceptance(h, timer, cfg, X, W, gathered, out, n: int, producers: int):
     """T_comp alone, T_comm alone and T_total (median ms) plus the consumers'
-    span inside the fused kernel, from the kernel's own %globaltimer stamps."""
+    span inside the fused kernel, from the kernel's own %globaltimer stamps.
+    `producers` is the handle's producer setting (0 = automatic split), put
+    back after the controls."""
     from consumer_movement_gemm_gb300 import tovl
     t_total = statistics.median(timer.time_calls(lambda: h.gather_gemm(X, W, gathered, out), n))
+    # the controls run with the fused call's split: C consumers alone, P producers alone
+    P, C = h.get_option(tovl.OPT_PRODUCERS), h.get_option(tovl.OPT_CONSUMERS)
+    h.set_option(tovl.OPT_PRODUCERS, P)
     t_comp = statistics.median(timer.time_calls(lambda: h.gemm_only(gathered, W, out), n))
     t_comm = statistics.median(timer.time_calls(lambda: h.copy_only(X, gathered), n))
+    assert h.get_option(tovl.OPT_CONSUMERS) == C
+    h.set_option(tovl.OPT_PRODUCERS, producers)
     h.set_option(tovl.OPT_STATS, 1)
     spans = []
     for _ in range(min(n, 20)):
@@ -319,7 +326,7 @@ def acceptance(h, timer, cfg, X, W, gathered, out, n: int):
         "T_comp_at_fused_ms": t_comp_fused,
         "overlap_efficiency": overlap, "overlap_target": 0.8,
         "compute_interference": t_comp_fused / t_comp, "interference_target": 1.1,
-        "producer_ctas": h.get_option(tovl.OPT_PRODUCERS), "consumer_ctas": h.get_option(tovl.OPT_CONSUMERS),
+        "producer_ctas": P, "consumer_ctas": C,
     }
 
 
@@ -355,7 +362,6 @@ def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int):
     """Dispatch + grouped GEMM: algorithmic TFLOP/s (real rows only)."""
     import numpy as np
     import torch
-    import oracle  # noqa: F401  (routing counts only come from the plan below)
     import workloads
     from consumer_movement_gemm_gb300 import tovl
     x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
@@ -455,7 +461,7 @@ def run_tovl(args):
     ms_max = max_over_ranks(ms, world)
     value = sum_over_ranks(cfg.flops, world) / (ms_max * 1e-3) / 1e12
 
-    acc = acceptance(h, timer, cfg, X, W, gathered, out, 50)
+    acc = acceptance(h, timer, cfg, X, W, gathered, out, 50, args.producers)
     e2e = e2e_tp(h, cfg, W, gathered, out, 50, stream)
 
     extra = {}
@@ -463,15 +469,15 @@ def run_tovl(args):
         sweep = []
         for P in [4, 8, 16, 24, 32]:
             h.set_option(tovl.OPT_PRODUCERS, P)
-            a = acceptance(h, timer, cfg, X, W, gathered, out, 30)
+            a = acceptance(h, timer, cfg, X, W, gathered, out, 30, P)
             a["TFLOP/s"] = cfg.flops / (a["T_total_ms"] * 1e-3) / 1e12
             sweep.append(a)
-        h.set_option(tovl.OPT_PRODUCERS, acc["producer_ctas"])
+        h.set_option(tovl.OPT_PRODUCERS, args.producers)
         extra["producer_sweep"] = sweep
         ks = []
         for S in [1, 2, 4, 8]:
             with tovl.Handle(local, max_rows=1 << 14, producer_ctas=acc["producer_ctas"], k_slices=S) as hs:
-                a = acceptance(hs, timer, cfg, X, W, gathered, out, 30)
+                a = acceptance(hs, timer, cfg, X, W, gathered, out, 30, acc["producer_ctas"])
                 a["k_slices"] = S
                 a["TFLOP/s"] = cfg.flops / (a["T_total_ms"] * 1e-3) / 1e12
                 ks.append(a)

@@ -136,13 +136,87 @@ __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s,
     if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
 }
 
-// TMA lane: wait until the gate warp has passed gate number `idx` (bounded).
+// Weight (B) cursor of the TMA lane.  B does not depend on the producers, so
+// its k-blocks are loaded ahead of the gate: a stage's B boxes are issued (and
+// the stage's full barrier armed for A + B bytes) as soon as the stage is
+// free, and the stage's A box follows once the slice's gate has passed.
 template <int PAIR>
-__device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, int idx)
+struct BCursor {
+    int t, kb, brow, n0;      // next k-block to load: tile, k-block, B row base, B column base
+    int issued;               // stages armed so far
+    uint32_t stage, phase;
+};
+
+template <int PAIR>
+__device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR>& sc, BCursor<PAIR>& b)
 {
+    if (b.t >= sc.n_tiles) return;
+    const int mb = sc.row_block(p, b.t);
+    b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
+    b.n0 = (b.t % p.n_nb) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+}
+
+// Arm the cursor's stage and issue its B boxes (the stage must be free).
+template <int PAIR>
+__device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                        BCursor<PAIR>& b)
+{
+    using T = Tile<PAIR>;
+    uint8_t* bdst = s.b + b.stage * T::kStageB;
+    if (PAIR == 1) {
+        ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
+#pragma unroll
+        for (int j = 0; j < T::kBBoxes; ++j)
+            ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
+                             b.brow + b.kb * kTileK);
+    } else {
+        // both CTAs' bytes are counted on the first CTA's barrier
+        if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
+        const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
+#pragma unroll
+        for (int j = 0; j < T::kBBoxes; ++j)
+            ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64, b.brow + b.kb * kTileK);
+    }
+    ++b.issued;
+    if (++b.stage == T::kStages) {
+        b.stage = 0;
+        b.phase ^= 1u;
+    }
+    if (++b.kb == p.n_kb) {
+        b.kb = 0;
+        b.t += sc.n_units;
+        b_tile<PAIR>(p, sc, b);
+    }
+}
+
+// Arm stages until the cursor is `ahead` stages past `a_count` (blocking on
+// free stages only when `block`).  Returns false on a pipeline timeout.
+template <int PAIR>
+__device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                      BCursor<PAIR>& b, int upto, bool block)
+{
+    while (b.issued < upto && b.t < sc.n_tiles) {
+        if (block) {
+            if (!mbar_wait(&s.empty[b.stage], b.phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return false;
+        } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
+            return true;
+        }
+        b_issue<PAIR>(p, s, sc, b);
+    }
+    return true;
+}
+
+// TMA lane: wait until the gate warp has passed gate number `idx` (bounded),
+// arming free stages with B meanwhile.
+template <int PAIR>
+__device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                          BCursor<PAIR>& b, int a_count, int idx)
+{
+    using T = Tile<PAIR>;
     if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
     const uint64_t start = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
+        if (!b_run<PAIR>(p, s, sc, b, a_count + T::kStages, false)) return false;
         if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
         if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
             record_error(p.ctrl, kErrTimeout);
@@ -152,53 +226,46 @@ __device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSm
     }
 }
 
-// TMA warp: per tile and K-slice, wait for the slice's gate, then stream A
-// and B k-blocks into the stage ring.  One lane issues everything.
+// TMA warp: per tile and K-slice, wait for the slice's gate, then stream the
+// slice's A k-blocks into stages whose B the cursor above has already
+// loaded.  One lane issues everything.
 template <int PAIR>
 __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
 {
     using T = Tile<PAIR>;
     if (ptx::lane_id() != 0) return;
-    uint32_t stage = 0, phase = 0;
+    BCursor<PAIR> b;
+    b.t = sc.unit;
+    b.kb = 0;
+    b.issued = 0;
+    b.stage = 0;
+    b.phase = 0;
+    b_tile<PAIR>(p, sc, b);
+    uint32_t stage = 0;
+    int a_count = 0;
     int gate_idx = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
         const int mb = sc.row_block(p, t);
-        const int nb = t % p.n_nb;
-        const int brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
-        const int n0 = nb * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
-                if (!wait_gate(p, s, gate_idx)) return;
+                if (!wait_gate<PAIR>(p, s, sc, b, a_count, gate_idx)) return;
                 // the rows were written through the generic proxy; order them
                 // before this thread's tensor-memory-access (async proxy) reads
                 ptx::fence_proxy_async_global();
             }
             const int kb1 = kb_begin(p, sl + 1);
             for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
-                if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
+                // this k-block's stage is armed and holds (or receives) its B
+                if (!b_run<PAIR>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
-                uint8_t* bdst = s.b + stage * T::kStageB;
                 if (PAIR == 1) {
-                    ptx::mbar_arrive_expect_tx(&s.full[stage], T::kStageBytes);
                     ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
-#pragma unroll
-                    for (int j = 0; j < T::kBBoxes; ++j)
-                        ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[stage], n0 + j * 64,
-                                         brow + kb * kTileK);
                 } else {
-                    // both CTAs' bytes are counted on the first CTA's barrier
-                    if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[stage], PAIR * T::kStageBytes);
                     const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
                     ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, mb * kTileM);
-#pragma unroll
-                    for (int j = 0; j < T::kBBoxes; ++j)
-                        ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, n0 + j * 64,
-                                              brow + kb * kTileK);
                 }
-                if (++stage == T::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                ++a_count;
+                if (++stage == T::kStages) stage = 0;
             }
         }
     }
@@ -269,6 +336,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
         if (!__all_sync(0xffffffffu, arrived)) return;
         ptx::tc_fence_after();
+        if (p.stats && lane == 0) {
+            const long long idx = static_cast<long long>(p.trace_tiles) * (p.k_slices + 1) + t;
+            if (idx < p.ctrl.trace_cap)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
         const int row = mb * kTileM + row_in_tile;
         const bool ok = row < valid_rows;
         const int col0 = half * (kTileN / 2);

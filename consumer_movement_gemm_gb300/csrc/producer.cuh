@@ -120,65 +120,132 @@ __device__ void seed_counters(const FusedParams& p, int gw, int n_gw, bool compl
     }
 }
 
-// Copy one item: item_rows destination rows x the K-slice's bytes, as one
-// flat range of 16-byte words walked 32 words per step, 16 words per lane in
-// flight.  A per-warp table in shared memory holds each row's source.
-__device__ __forceinline__ int copy_item(const FusedParams& p, const Item& it, const uint8_t** tbl)
+// Lane layout of one item.  An item is RI rows x n16 16-byte words; G rows
+// are copied at once, L = 32 / G lanes per row, each lane owning M = RI / G
+// rows (M > 1 only when RI > 16).  Lane l copies words lo, lo + L, lo + 2L,
+// ... of rows lr + G*m (lr = l / L, lo = l % L): every group of L lanes moves
+// L x 16 contiguous bytes (at least one full 32-byte sector) per instruction,
+// each lane keeps one source and one destination pointer per row, and the
+// word offsets of a pass are compile-time multiples of L x 16 bytes.
+template <int M>
+struct ItemState {
+    Item it;
+    const uint8_t* src[M];   // this lane's rows (a readable dummy where a row has no source)
+    uint8_t* dst[M];
+    bool has[M];             // the row has a source
+    int n16;                 // 16-byte words per row slice
+    int counter;
+    int n;                   // rows of this item that have a source
+};
+
+template <int M>
+struct LaneMap {
+    int RI, G, L, lr, lo;
+    __device__ LaneMap(int ri, int lane)
+    {
+        RI = ri;
+        G = ri / M;
+        L = 32 / G;
+        lr = lane / L;
+        lo = lane - lr * L;
+    }
+};
+
+// Decode item i and resolve this lane's rows.
+template <int M>
+__device__ __forceinline__ ItemState<M> begin_item(const FusedParams& p, const LaneMap<M>& lm, int i, int n_blocks)
 {
-    const uint32_t lane = ptx::lane_id();
-    const int RI = p.item_rows;
-    for (int l = lane; l < RI; l += 32) tbl[l] = row_src(p, it.r0 + l);
-    __syncwarp();
-    const size_t soff = static_cast<size_t>(kb_begin(p, it.s)) * kTileK * 2;
-    const int n16 = (kb_begin(p, it.s + 1) - kb_begin(p, it.s)) * kTileK * 2 / 16;
-    uint8_t* dst = static_cast<uint8_t*>(p.gathered) + soff + static_cast<size_t>(it.r0) * p.row_bytes;
-    // lane position (row, col) in the item's flat range, advanced by 32 words
-    // per step without division
-    int row = static_cast<int>(lane) / n16;
-    int col = static_cast<int>(lane) - row * n16;
-    while (row < RI) {
-        int4 v[kItemInt4 / 32];
-        int r = row, c = col;
+    const int lane = static_cast<int>(ptx::lane_id());
+    const uint8_t* dummy = static_cast<const uint8_t*>(p.mode == kModeGather ? p.shard[0] : p.x);
+    ItemState<M> st;
+    st.it = decode_item(p, i, n_blocks);
+    const size_t soff = static_cast<size_t>(kb_begin(p, st.it.s)) * kTileK * 2;
+    st.n16 = (kb_begin(p, st.it.s + 1) - kb_begin(p, st.it.s)) * kTileK * 2 / 16;
+    st.counter = (p.mode == kModeGather) ? (st.it.r0 / kChunkRows) * p.ctrl.n_slices + st.it.s
+                                         : st.it.mb * p.ctrl.n_slices + st.it.s;
+    // lanes l < RI resolve rows l and l + 32; the row owners read them by shuffle
+    const uint8_t* s0 = lane < lm.RI ? row_src(p, st.it.r0 + lane) : nullptr;
+    const uint8_t* s1 = lane + 32 < lm.RI ? row_src(p, st.it.r0 + lane + 32) : nullptr;
+    st.n = __popc(__ballot_sync(0xffffffffu, s0 != nullptr)) + __popc(__ballot_sync(0xffffffffu, s1 != nullptr));
 #pragma unroll
-        for (int j = 0; j < kItemInt4 / 32; ++j) {
-            if (r < RI) {
-                const uint8_t* src = tbl[r];
-                if (src) v[j] = ptx::ld_nc_v4(reinterpret_cast<const int4*>(src + soff) + c);
-            }
-            c += 32;
-            while (c >= n16) {
-                c -= n16;
-                ++r;
-            }
-        }
-        r = row;
-        c = col;
+    for (int m = 0; m < M; ++m) {
+        const int r = lm.lr + lm.G * m;
+        const unsigned long long a0 = __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s0), r & 31);
+        const unsigned long long a1 = __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s1), r & 31);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(r < 32 ? a0 : a1);
+        st.has[m] = src != nullptr;
+        st.src[m] = src ? src + soff : dummy;
+        st.dst[m] = static_cast<uint8_t*>(p.gathered) + static_cast<size_t>(st.it.r0 + r) * p.row_bytes + soff;
+    }
+    return st;
+}
+
+// Pass `ps` over an item: 16 words per lane.  Loads are unconditional (a
+// word outside the item reads the row's first word, or the dummy row): a
+// conditional load into a live register must be merged with the old value,
+// which makes every load wait for the one before it.
+template <int M>
+__device__ __forceinline__ void load_pass(const ItemState<M>& st, const LaneMap<M>& lm, int ps,
+                                          int4 (&v)[kItemInt4 / 32])
+{
+    constexpr int QN = kItemInt4 / 32 / M;    // words per row per lane and pass
 #pragma unroll
-        for (int j = 0; j < kItemInt4 / 32; ++j) {
-            if (r < RI && tbl[r]) ptx::st_v4(reinterpret_cast<int4*>(dst + static_cast<size_t>(r) * p.row_bytes) + c, v[j]);
-            c += 32;
-            while (c >= n16) {
-                c -= n16;
-                ++r;
-            }
+    for (int k = 0; k < kItemInt4 / 32; ++k) {
+        const int m = k / QN, q = k % QN;
+        const int c = lm.lo + lm.L * (ps * QN + q);
+        const int4* a = reinterpret_cast<const int4*>(st.src[m]) + (c < st.n16 ? c : 0);
+        v[k] = ptx::ld_nc_v4(a);
+    }
+}
+
+template <int M>
+__device__ __forceinline__ void store_pass(const ItemState<M>& st, const LaneMap<M>& lm, int ps,
+                                           const int4 (&v)[kItemInt4 / 32])
+{
+    constexpr int QN = kItemInt4 / 32 / M;
+#pragma unroll
+    for (int k = 0; k < kItemInt4 / 32; ++k) {
+        const int m = k / QN, q = k % QN;
+        const int c = lm.lo + lm.L * (ps * QN + q);
+        if (st.has[m] && c < st.n16) ptx::st_v4(reinterpret_cast<int4*>(st.dst[m]) + c, v[k]);
+    }
+}
+
+template <int M>
+__device__ void copy_items(const FusedParams& p, int gw, int n_gw)
+{
+    const int lane = static_cast<int>(ptx::lane_id());
+    const LaneMap<M> lm(p.item_rows, lane);
+    const int n_blocks = num_row_blocks(p);
+    const int n_items = n_blocks * p.k_slices * (kBlockRows / p.item_rows);
+    // words a lane covers per pass, per row: QN words L apart
+    const int per_pass = lm.L * (kItemInt4 / 32 / M);
+    // Every item is released as soon as it is copied: a warp's consecutive
+    // items are n_gw items apart in the consumers' order, so holding one back
+    // to share a release fence would delay an earlier K-slice behind later
+    // ones (measured: batching four items cost 12 us of the TP fused call and
+    // saved no copy time).  Issuing the next item's loads before this item's
+    // release was measured too: the release then also waits for those loads,
+    // and the first chunks publish later.
+    for (int i = gw; i < n_items; i += n_gw) {
+        const ItemState<M> st = begin_item<M>(p, lm, i, n_blocks);
+        const int passes = (st.n16 + per_pass - 1) / per_pass;
+        for (int ps = 0; ps < passes; ++ps) {
+            int4 v[kItemInt4 / 32];
+            load_pass<M>(st, lm, ps, v);
+            store_pass<M>(st, lm, ps, v);
         }
-        row = r;
-        col = c;
+        // the copies above happen-before lane 0's release below
+        __syncwarp();
+        if (lane == 0 && st.n > 0) item_done(p, st.counter, st.n);
+        __syncwarp();
     }
-    // rows this item filled
-    int n = 0;
-    for (int l = 0; l < RI; l += 32) {
-        const bool real = (l + static_cast<int>(lane) < RI) && tbl[l + lane] != nullptr;
-        n += __popc(__ballot_sync(0xffffffffu, real));
-    }
-    __syncwarp();
-    return n;
 }
 
 __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
 {
+    (void)smem;
     const int warp = threadIdx.x / 32;
-    const uint32_t lane = ptx::lane_id();
     const int n_warps = kThreads / 32;
     // consecutive items go to different CTAs (SMs), so the rows of one chunk
     // are copied by many SMs at once
@@ -186,25 +253,9 @@ __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
     const int n_gw = p.n_producers * n_warps;
     if (threadIdx.x == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
     seed_counters(p, gw, n_gw, true);
-
-    const uint8_t** tbl = reinterpret_cast<const uint8_t**>(smem) + warp * 64;   // row-source table per warp
-    const int n_blocks = num_row_blocks(p);
-    const int n_items = n_blocks * p.k_slices * (kBlockRows / p.item_rows);
-    const int S = p.ctrl.n_slices;
-    // Every item is released as soon as it is copied: a warp's consecutive
-    // items are n_gw items apart in the consumers' order, so holding one back
-    // to share a release fence would delay an earlier K-slice behind later
-    // ones (measured: batching four items cost 12 us of the TP fused call and
-    // saved no copy time).
-    for (int i = gw; i < n_items; i += n_gw) {
-        const Item it = decode_item(p, i, n_blocks);
-        const int n = copy_item(p, it, tbl);
-        const int counter = (p.mode == kModeGather) ? (it.r0 / kChunkRows) * S + it.s : it.mb * S + it.s;
-        // the copies above happen-before lane 0's release below
-        __syncwarp();
-        if (lane == 0 && n > 0) item_done(p, counter, n);
-        __syncwarp();
-    }
+    if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
+    else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
+    else copy_items<4>(p, gw, n_gw);
     seed_counters(p, gw, n_gw, false);
     __syncwarp();
     __syncthreads();

@@ -49,10 +49,12 @@ __device__ __forceinline__ bool arrive_and_publish(const Ctrl& ctrl, int c, int 
 
 // Bounded wait of one warp until every watched word is >= target.
 // Lane i watches words[i] (lanes >= n watch nothing).  Polls use acquire
-// loads; the warp decides with a ballot.  On success lane 0 itself holds an
-// acquire observation of every word (it re-reads them), so lane 0 may issue
-// the dependent reads.  Returns the number of polling rounds, negative on
-// timeout or abort.
+// loads; the warp decides with a vote.  The lane that saw a word reach the
+// target holds an acquire observation of it; the warp barrier after the vote
+// orders every lane's observation before whatever any lane of the warp does
+// next (bar.warp.sync orders memory among its threads), so lane 0 may hand
+// the gate on without reading the words again.  Returns the number of
+// polling rounds, negative on timeout or abort.
 __device__ __forceinline__ int warp_wait_ge(const int* const* words, int n, int target, const Ctrl& ctrl, int seq,
                                             long long timeout_ns)
 {
@@ -83,24 +85,8 @@ __device__ __forceinline__ int warp_wait_ge(const int* const* words, int n, int 
         __nanosleep(backoff);
         if (backoff < 256) backoff <<= 1;
     }
-    // The words are monotonic and every lane already saw them reach the
-    // target, so these re-reads succeed at once; the bound is only a guard.
-    int ok0 = 1;
-    if (lane == 0) {
-        for (int i = 0; i < n; ++i) {
-            int tries = 0;
-            while (ptx::ld_acquire_gpu(words[i]) < target) {
-                if (++tries > (1 << 20)) {
-                    record_error(ctrl, kErrTimeout);
-                    raise_abort(ctrl, seq);
-                    ok0 = 0;
-                    break;
-                }
-            }
-        }
-    }
-    ok0 = __shfl_sync(0xffffffffu, ok0, 0);
-    return ok0 ? rounds : -rounds;
+    __syncwarp();
+    return rounds;
 }
 
 // Bounded mbarrier wait (intra-CTA pipelines).  These only depend on this

@@ -394,7 +394,7 @@ static int reset_stats(tovl_ctx* h, cudaStream_t s, long long tiles, int ks)
     if (!h->stats) return TOVL_OK;
     // min slots start at all-ones, the others at zero; the timeline at zero
     cudaError_t e = cudaMemsetAsync(h->ctrl.stats, 0, kNumStats * sizeof(unsigned long long), s);
-    long long n_trace = tiles * (ks + 1);
+    long long n_trace = tiles * (ks + 2);
     if (n_trace > h->ctrl.trace_cap) n_trace = h->ctrl.trace_cap;
     if (e == cudaSuccess && n_trace > 0) e = cudaMemsetAsync(h->ctrl.trace, 0, n_trace * sizeof(long long), s);
     if (e == cudaSuccess)
@@ -728,6 +728,9 @@ TOVL_API int tovl_read_trace(tovl_handle h, int what, long long* out, long long 
     } else if (what == 2) {
         src = h->ctrl.trace + h->last_tiles * h->last_ks;
         avail = h->last_tiles;
+    } else if (what == 3) {
+        src = h->ctrl.trace + h->last_tiles * (h->last_ks + 1);
+        avail = h->last_tiles;
     } else {
         return TOVL_ERR_INVALID;
     }
@@ -755,7 +758,7 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
     if (!h) return TOVL_ERR_INVALID;
     switch (option) {
     case 1:
-        if (value < 1 || value >= h->num_sms) return TOVL_ERR_INVALID;
+        if (value < 0 || value >= h->num_sms) return TOVL_ERR_INVALID;
         h->producers = static_cast<int>(value);
         return TOVL_OK;
     case 2:

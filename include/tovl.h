@@ -216,7 +216,8 @@ int tovl_read_ctrl(tovl_handle h, int* slots, int* cnts, int* rbcnts, long long*
  * Any pointer may be NULL. */
 int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* pad, int* blk_expert, int* m_pad);
 
-/* Options for sweeps: 1 = producer CTAs, 2 = consumer CTAs, 3 = copy mode,
+/* Options for sweeps: 1 = producer CTAs (0 = automatic split; reads back
+ * the count the last call used), 2 = consumer CTAs, 3 = copy mode,
  * 4 = statistics on/off, 5 = wait timeout in ns, 6 = copy-sweep CTAs,
  * 7 = copy-sweep waiter CTAs, 9 = k_slices (read only),
  * 10 = CTA-pair consumers for gather calls (1 = on, the default: two CTAs of a
@@ -244,6 +245,7 @@ int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n);
  *           (0 where no producer thread published it)
  *   what 1: time the consumer's gate passed each (tile, slice) [tiles*k_slices]
  *   what 2: time each tile's output was stored [tiles]
+ *   what 3: time each tile's accumulator was complete (epilogue start) [tiles]
  * Tiles are numbered row block * (N/256) + column block; for dispatch calls
  * the tile count is the bound tovl_dispatch_rows/128 * N/256 (unused tiles
  * read 0).  n must not exceed the stated length. */
