@@ -30,20 +30,23 @@ namespace tovl {
 
 template <int PAIR>
 struct Tile {
-    static constexpr int kStages = PAIR == 1 ? 4 : 6;
+    static constexpr int kStages = stages_for(PAIR);
     static constexpr int kStageA = kTileM * kTileK * 2;               // 16 KB
     static constexpr int kStageB = kTileK * kTileN * 2 / PAIR;        // this CTA's B columns
     static constexpr int kStageBytes = kStageA + kStageB;
     static constexpr int kBBoxes = kTileN / 64 / PAIR;                // 64-column TMA boxes per stage
     // M = 128 * PAIR, N = 256, A K-major, B MN-major (W is [K][N], N contiguous)
     static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM * PAIR, kTileN, false, true);
-    static_assert(kStages * kStageBytes + 1024 <= kSmemBytes, "stages must fit the dynamic shared memory");
+    static_assert(kStages * kStageBytes + kEpiWarps * kEpiBufBytes + 1024 <= smem_bytes(PAIR),
+                  "stages and epilogue buffers must fit the dynamic shared memory");
+    static_assert(smem_bytes(PAIR) <= 227 * 1024, "at most 227 KB of shared memory per CTA");
 };
 
 template <int PAIR>
 struct ConsumerSmem {
     uint8_t* a;          // kStages x [128 rows][128 B]  (A tile, 128B swizzle)
     uint8_t* b;          // kStages x kBBoxes x [64 k-rows][128 B]  (this CTA's B columns)
+    uint8_t* epi;        // kEpiWarps x [32 rows][64 B] output staging (64B swizzle)
     uint64_t* full;      // TMA -> MMA (in the pair's first CTA: counts both CTAs' bytes)
     uint64_t* empty;     // MMA -> TMA
     uint64_t* tfull;     // MMA -> epilogue (per accumulator)
@@ -59,7 +62,8 @@ __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
     ConsumerSmem<PAIR> s;
     s.a = smem;
     s.b = smem + T::kStages * T::kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kStages * T::kStageBytes);
+    s.epi = smem + T::kStages * T::kStageBytes;   // 1024-byte aligned: stages are multiples of 1 KB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + kEpiWarps * kEpiBufBytes);
     s.full = bars;
     s.empty = bars + T::kStages;
     s.tfull = bars + 2 * T::kStages;
@@ -314,19 +318,27 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     }
 }
 
-// Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) -> out.
-// Warp w reads TMEM lane quarter w % 4 (the quarter its position allows) and
-// one half of the 256 accumulator columns.
+// Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) ->
+// shared memory -> TMA tensor store.  Warp w reads TMEM lane quarter w % 4
+// (the quarter its position allows), i.e. 32 output rows, and one half of
+// the 256 accumulator columns, as four 32 x 32 boxes.  A box is written into
+// the warp's 2 KB buffer in the 64-byte swizzled layout the store's tensor
+// map expects (16-byte chunk j of 64-byte row r at chunk j ^ ((r / 2) % 4):
+// the eight rows a quarter-warp writes hit distinct banks), then one lane
+// stores it; rows past the output's extent (the ragged tail of M) are
+// clipped by the store.  The accumulator is released as soon as its last
+// columns are in registers.
 template <int PAIR>
 __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
-                                  uint32_t tmem_base, int valid_rows)
+                                  uint32_t tmem_base)
 {
     const int warp = threadIdx.x / 32;
     const uint32_t lane = ptx::lane_id();
     const int q = warp & 3;
     const int half = (warp - kEpiWarp0) / 4;
-    const int row_in_tile = q * 32 + static_cast<int>(lane);
-    uint16_t* out = static_cast<uint16_t*>(p.out);
+    const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
+    const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
+    const uint32_t swz = (lane >> 1) & 3u;
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const int mb = sc.row_block(p, t);
@@ -334,48 +346,60 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
-        if (!__all_sync(0xffffffffu, arrived)) return;
+        if (!__all_sync(0xffffffffu, arrived)) break;
         ptx::tc_fence_after();
         if (p.stats && lane == 0) {
             const long long idx = static_cast<long long>(p.trace_tiles) * (p.k_slices + 1) + t;
             if (idx < p.ctrl.trace_cap)
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
         }
-        const int row = mb * kTileM + row_in_tile;
-        const bool ok = row < valid_rows;
-        const int col0 = half * (kTileN / 2);
-        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * p.N + nb * kTileN + col0);
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + col0;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
 #pragma unroll 1
-        for (int c = 0; c < kTileN / 2 / 32; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-            ptx::tmem_ld_wait();
-            if (ok) {
+        for (int bx = 0; bx < kTileN / 2 / kEpiBoxCols; ++bx) {
+            // the previous store from this buffer has finished reading it
+            if (lane == 0) ptx::bulk_wait_read<0>();
+            __syncwarp();
+            {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + bx * kEpiBoxCols, r);
+                ptx::tmem_ld_wait();
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                    w.y = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                    w.z = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                    w.w = ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                    dst[c * 4 + v] = w;
+                    const uint32_t chunk = static_cast<uint32_t>(v) ^ swz;
+                    ptx::st_shared_v4(row_addr + chunk * 16,
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
                 }
             }
-        }
-        // this warp's reads of the accumulator are done: one arrival per warp
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            if (PAIR == 1) ptx::mbar_arrive(&s.tempty[acc]);
-            else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
-            if (p.stats) {
-                const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
-                if (idx < p.ctrl.trace_cap)
-                    atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+            if (bx == kTileN / 2 / kEpiBoxCols - 1) {
+                // this warp's reads of the accumulator are done: one arrival per warp
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (PAIR == 1) ptx::mbar_arrive(&s.tempty[acc]);
+                    else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
+                }
+            }
+            // the box's generic-proxy writes are visible to the tensor store
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                  mb * kTileM + q * 32);
+                ptx::bulk_commit();
             }
         }
+        if (p.stats && lane == 0) {
+            const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
+            if (idx < p.ctrl.trace_cap)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
     }
+    // every store has written global memory before the CTA retires
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
 }
 
 template <int PAIR>
@@ -398,6 +422,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
         ptx::prefetch_tmap(&p.tmap_b);
+        ptx::prefetch_tmap(&p.tmap_out);
         stat_min(p, kStatConsStartNs, ptx::globaltimer());
     }
     if (warp == 1) {
@@ -417,10 +442,9 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
 
-    const int valid_rows = (p.mode == kModeGather) ? p.M : p.meta[0];
     if (warp == 0) consumer_tma<PAIR>(p, s, sc);
     else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
-    else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base, valid_rows);
+    else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
     else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
     __syncwarp();
 

@@ -26,6 +26,7 @@ constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
 constexpr int kTraceCap = 1 << 20; // timeline entries kept when statistics are on
 constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
 constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)
+constexpr int kItemBytes = kItemInt4 * 16;
 constexpr int kMaxShards = 64;
 constexpr int kMaxK = 32768;       // a producer ring stage must hold one 64 KB row
 constexpr int kMaxExperts = 512;
@@ -35,7 +36,20 @@ constexpr int kStageB = kTileK * kTileN * 2;      // 32 KB
 constexpr int kStageBytes = kStageA + kStageB;    // 48 KB
 constexpr int kTmemCols = 512;                    // two 128x256 fp32 accumulators
 // dynamic shared memory: stages + barriers + 1 KB alignment slack
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+constexpr int kEpiBoxCols = 32;                   // output box of one epilogue store: 32 rows x 32 columns
+constexpr int kEpiBufBytes = 32 * kEpiBoxCols * 2; // 2 KB staging buffer per epilogue warp (64B swizzle)
+constexpr int kPairStages = 5;                     // pipeline stages of a CTA-pair consumer (32 KB each)
+
+// Pipeline stages and dynamic shared memory of the fused kernel per consumer
+// shape.  Producer CTAs share the launch's shared-memory size, and a producer
+// SM's L1 is what is left of the 256 KB: every kilobyte given to shared
+// memory is one its loads cannot have in flight, so the stages are as few as
+// keep the tensor pipe fed.
+constexpr int stages_for(int pair) { return pair == 1 ? kStages : kPairStages; }
+constexpr int smem_bytes(int pair)
+{
+    return stages_for(pair) * (kStageA + kStageB / pair) + kEpiWarps * kEpiBufBytes + 1024 + 1024;
+}
 
 // Device status codes (mirror tovl.h).
 enum : int {
@@ -93,6 +107,7 @@ enum : int { kModeGather = 0, kModeDispatch = 1 };
 struct FusedParams {
     CUtensorMap tmap_a;   // A: gathered / dispatched rows [rows][K] bf16, box 64 x 128, 128B swizzle
     CUtensorMap tmap_b;   // B: weights [(E*)K][N] bf16 row-major (MN-major operand), box 64 x 64
+    CUtensorMap tmap_out; // out [rows][N] bf16, box 32 x 32, 64B swizzle (rows past the extent are not stored)
     int mode;
     int M;                // gather: rows of the gathered buffer
     int N, K;
@@ -110,6 +125,7 @@ struct FusedParams {
     int k_slices;         // K-slices in use this call (<= ctrl.n_slices); slices beyond are seeded
     int wave_blocks;      // row blocks the consumers' first wave covers (producer ordering group)
     int item_rows;        // rows per producer item (a power of two dividing 64)
+    int producer_mode;    // 0: vector copies through registers; 1: bulk loads staged in shared memory
     int trace_tiles;      // tile count bound that lays out the timeline (gate times, then end times)
     // gather sources
     const void* shard[kMaxShards];

@@ -47,7 +47,7 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(grid);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = kSmemBytes;
+    lc.dynamicSmemBytes = smem_bytes(pair);
     lc.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -68,16 +68,16 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
 
 cudaError_t prepare_fused()
 {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
     return e;
 }
 
 int fused_max_active_per_sm()
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kThreads, kSmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kThreads, smem_bytes(1)) != cudaSuccess)
         return 0;
     return n;
 }
@@ -87,7 +87,7 @@ int fused_max_active_pairs()
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = kSmemBytes;
+    lc.dynamicSmemBytes = smem_bytes(2);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;

@@ -242,9 +242,71 @@ __device__ void copy_items(const FusedParams& p, int gw, int n_gw)
     }
 }
 
+// Staged variant: each warp owns an 8 KB shared-memory buffer and an
+// mbarrier.  Per pass, the lanes that own rows issue bulk asynchronous loads
+// of their row segments into the buffer (completion counted in bytes on the
+// warp's mbarrier); the warp waits, then writes the buffer out with 16-byte
+// vector stores in the lane layout above.  The loads in flight live in the
+// producer CTA's shared memory, which it has no other use for, instead of
+// in L1.
+template <int M>
+__device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, int n_gw)
+{
+    const int lane = static_cast<int>(ptx::lane_id());
+    const int warp = threadIdx.x / 32;
+    uint8_t* buf = smem + warp * kItemBytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (kThreads / 32) * kItemBytes) + warp;
+    if (lane == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    uint32_t phase = 0;
+    const LaneMap<M> lm(p.item_rows, lane);
+    const int RI = p.item_rows;
+    const int n_blocks = num_row_blocks(p);
+    const int n_items = n_blocks * p.k_slices * (kBlockRows / RI);
+    constexpr int QN = kItemInt4 / 32 / M;
+    for (int i = gw; i < n_items; i += n_gw) {
+        const ItemState<M> st = begin_item<M>(p, lm, i, n_blocks);
+        const size_t soff = static_cast<size_t>(kb_begin(p, st.it.s)) * kTileK * 2;
+        const int passes = (st.n16 + kItemInt4 - 1) / kItemInt4;   // > 1 only for single-row items
+        for (int ps = 0; ps < passes && st.n > 0; ++ps) {
+            const int words = min(st.n16 - ps * kItemInt4, kItemInt4 / RI);   // 16-byte words per row this pass
+            const uint32_t seg = static_cast<uint32_t>(words) * 16;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(st.n) * seg);
+            __syncwarp();
+            for (int l = lane; l < RI; l += 32) {
+                const uint8_t* src = row_src(p, st.it.r0 + l);
+                if (src) ptx::bulk_load(buf + l * seg, src + soff + static_cast<size_t>(ps) * kItemBytes, seg, bar);
+            }
+            const bool ok = mbar_wait(bar, phase, p.ctrl, p.pipe_timeout_ns);
+            phase ^= 1u;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            const uint32_t base = ptx::smem_u32(buf);
+#pragma unroll
+            for (int k = 0; k < kItemInt4 / 32; ++k) {
+                const int m = k / QN, q = k % QN;
+                const int r = lm.lr + lm.G * m;
+                const int c = lm.lo + lm.L * q;
+                if (st.has[m] && c < words) {
+                    const int4 v = ptx::ld_shared_v4(base + static_cast<uint32_t>(r) * seg + c * 16);
+                    ptx::st_v4(reinterpret_cast<int4*>(st.dst[m]) + ps * kItemInt4 + c, v);
+                }
+            }
+            // the buffer's generic reads come before the next pass's bulk writes
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+        }
+        // the copies above happen-before lane 0's release below
+        __syncwarp();
+        if (lane == 0 && st.n > 0) item_done(p, st.counter, st.n);
+        __syncwarp();
+    }
+}
+
 __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
 {
-    (void)smem;
     const int warp = threadIdx.x / 32;
     const int n_warps = kThreads / 32;
     // consecutive items go to different CTAs (SMs), so the rows of one chunk
@@ -253,9 +315,15 @@ __device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
     const int n_gw = p.n_producers * n_warps;
     if (threadIdx.x == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
     seed_counters(p, gw, n_gw, true);
-    if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
-    else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
-    else copy_items<4>(p, gw, n_gw);
+    if (p.producer_mode == 1) {
+        if (p.item_rows <= 16) copy_items_staged<1>(p, smem, gw, n_gw);
+        else if (p.item_rows == 32) copy_items_staged<2>(p, smem, gw, n_gw);
+        else copy_items_staged<4>(p, smem, gw, n_gw);
+    } else {
+        if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
+        else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
+        else copy_items<4>(p, gw, n_gw);
+    }
     seed_counters(p, gw, n_gw, false);
     __syncwarp();
     __syncthreads();

@@ -41,6 +41,7 @@ struct tovl_ctx {
     int max_pairs = 0;       // co-resident CTA pairs of the pair kernel on this device
     bool coop_pairs = true;  // cooperative launch accepted together with clusters
     bool coop_enabled = true;  // fused launches ask for the co-residency guarantee
+    int producer_mode = 0;     // fused producers: 0 vector copies, 1 staged bulk loads
     long long seq = 0;
     Ctrl ctrl{};
     Plan plan{};
@@ -285,14 +286,15 @@ TOVL_API int tovl_num_sms(tovl_handle h)
 // rows `stride` bytes apart; boxes of box_inner x box_outer, 128B swizzle,
 // out-of-range elements read as zero.
 static int encode_2d(tovl_ctx* h, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                     uint64_t stride, uint32_t box_inner, uint32_t box_outer)
+                     uint64_t stride, uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {stride};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         std::snprintf(h->last_error, sizeof h->last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -314,6 +316,7 @@ static void base_params(tovl_ctx* h, FusedParams& p)
     p.timeout_ns = h->timeout_ns;
     p.pipe_timeout_ns = pipe_timeout(h);
     p.stats = h->stats;
+    p.producer_mode = h->producer_mode;
     p.ctrl = h->ctrl;
 }
 
@@ -440,10 +443,12 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     p.n_kb = K / kTileK;
     p.n_nb = N / kTileN;
     p.row_bytes = K * 2;
-    // the split (and with it P for copy-only and C for GEMM-only) is the one
-    // the fused call uses; only launches with consumers need CTA pairs
-    const int split_pair = (h->pair_mode && h->max_pairs > 0) ? 2 : 1;
-    const int pair = (flags & 2) ? split_pair : 1;
+    // the split (and with it P for copy-only and C for GEMM-only) and the
+    // kernel shape are the ones the fused call uses, so the controls run
+    // under the same launch (shared-memory size, and with it the producer
+    // SMs' L1 share)
+    const int pair = (h->pair_mode && h->max_pairs > 0) ? 2 : 1;
+    const int split_pair = pair;
     const int n_mb = (M + kTileM - 1) / kTileM;
     int P, C;
     split_ctas(h, P, C, n_mb, p.n_nb, 4.0 * M * K, 2.0 * M * static_cast<double>(N) * K, split_pair);
@@ -461,6 +466,9 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     if (flags & 2) {
         if ((rc = encode_2d(h, &p.tmap_a, A, K, M, static_cast<uint64_t>(K) * 2, kTileK, kTileM)) != TOVL_OK) return rc;
         if ((rc = encode_2d(h, &p.tmap_b, W, N, K, static_cast<uint64_t>(N) * 2, 64, kTileK)) != TOVL_OK) return rc;
+        if ((rc = encode_2d(h, &p.tmap_out, out, N, M, static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
+            return rc;
     }
     const bool round = (flags & 1) != 0;
     if (round) p.seq = static_cast<int>(h->seq + 1);
@@ -575,6 +583,9 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
         return rc;
     if ((rc = encode_2d(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(N) * 2, 64, kTileK)) !=
         TOVL_OK)
+        return rc;
+    if ((rc = encode_2d(h, &p.tmap_out, out, N, rows, static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32,
+                        CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
         return rc;
     p.seq = static_cast<int>(h->seq + 1);
     p.gate_seq = p.seq + h->fault_gate_offset;
@@ -796,6 +807,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != 0 && value != 1) return TOVL_ERR_INVALID;
         h->coop_enabled = value != 0;
         return TOVL_OK;
+    case 14:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->producer_mode = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -818,6 +833,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 11: *value = h->max_pairs; return TOVL_OK;
     case 12: *value = h->coop_pairs ? 1 : 0; return TOVL_OK;
     case 13: *value = h->coop_enabled ? 1 : 0; return TOVL_OK;
+    case 14: *value = h->producer_mode; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

@@ -37,6 +37,7 @@ OPT_PAIRS = 10
 OPT_MAX_PAIRS = 11
 OPT_COOP_PAIRS = 12
 OPT_COOPERATIVE = 13
+OPT_PRODUCER_MODE = 14
 
 
 class TovlError(RuntimeError):

@@ -54,7 +54,7 @@ typedef enum {
 } tovl_status;
 
 /* Row-copy mechanism of tovl_gated_copy.  The producers of the fused
- * kernels always use 16-byte vector copies by 12 warps per CTA. */
+ * kernels use 16 warps per CTA; their copy path is option 14. */
 typedef enum {
     TOVL_COPY_VECTOR = 0,      /* 16-byte vector loads/stores by warps */
     TOVL_COPY_BULK = 1         /* bulk asynchronous copies through a shared-memory ring */
@@ -228,6 +228,10 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * launches request the cooperative co-residency guarantee (1, the default;
  * 0 launches the same kernel without it, for tools that cannot replay
  * cooperative launches -- the grid still fits one CTA per SM),
+ * 14 = producer copy path of the fused kernels: 0 = 16-byte vector loads and
+ * stores through registers (the default), 1 = bulk asynchronous loads of each
+ * row segment into a per-warp shared-memory buffer, then 16-byte vector
+ * stores (results are identical),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

@@ -86,10 +86,12 @@ def _gather_round(h, cfg, seed):
 
 @pytest.mark.parametrize("k_slices", [1, 2, 4, 8])
 @pytest.mark.parametrize("pairs", [1, 0])
-def test_tiny_gather_gemm_three_rounds(k_slices, pairs):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tiny_gather_gemm_three_rounds(k_slices, pairs, mode):
     cfg = workloads.TINY
     with _handle(k_slices=k_slices) as h:
         h.set_option(tovl.OPT_PAIRS, pairs)
+        h.set_option(tovl.OPT_PRODUCER_MODE, mode)
         if pairs:
             assert h.get_option(tovl.OPT_PAIRS) == 1, "CTA pairs unavailable on this device"
         for r in range(1, cfg.rounds + 1):
@@ -102,13 +104,18 @@ def test_tiny_gather_gemm_three_rounds(k_slices, pairs):
             _check_ctrl(h, r)
 
 
+# item shapes: (3,100,192) 32-row items; (1,64,64) 64-row items; (2,70,8192,KS=1)
+# single-row items wider than one 8 KB pass
 @pytest.mark.parametrize("S,R,K,N,P,KS", [(3, 100, 192, 256, 4, 2), (1, 64, 64, 512, 1, 4), (5, 77, 128, 256, 32, 1),
-                                          (2, 200, 320, 256, 8, 4), (7, 33, 448, 512, 3, 8)])
+                                          (2, 200, 320, 256, 8, 4), (7, 33, 448, 512, 3, 8),
+                                          (2, 70, 8192, 256, 4, 1)])
 @pytest.mark.parametrize("pairs", [1, 0])
-def test_gather_gemm_ragged(S, R, K, N, P, KS, pairs):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_gather_gemm_ragged(S, R, K, N, P, KS, pairs, mode):
     cfg = workloads.GatherCfg("ragged", S, R, K, N, rounds=2)
     with _handle(producer_ctas=P, k_slices=KS) as h:
         h.set_option(tovl.OPT_PAIRS, pairs)
+        h.set_option(tovl.OPT_PRODUCER_MODE, mode)
         for r in range(1, 3):
             X, W, gathered, out = _gather_round(h, cfg, 100 + r)
             assert h.sync_status() == 0
@@ -194,9 +201,11 @@ ROUTINGS = {
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
 @pytest.mark.parametrize("k_slices", [1, 2])
-def test_dispatch_grouped_gemm_small(routing, k_slices):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_dispatch_grouped_gemm_small(routing, k_slices, mode):
     H, N = 192, 256
     with _handle(k_slices=k_slices) as h:
+        h.set_option(tovl.OPT_PRODUCER_MODE, mode)
         for r in range(1, 4):
             topk_np, E = ROUTINGS[routing](workloads.round_seed(1, r))
             T = topk_np.shape[0]
