@@ -57,6 +57,7 @@ def _load():
                 "oracle_gather": ([P, I, I, I, P], None),
                 "oracle_dispatch": ([P, I, I, P, I, L, P], None),
                 "oracle_copy_perm": ([P, L, I, P, P], None),
+                "oracle_combine": ([P, I, P, P, I, I, P, P], None),
                 "oracle_matmul_f32": ([P, P, I, I, I, P], None),
                 "oracle_matmul_rows_f32": ([P, P, I, I, P, I, P], None),
                 "oracle_grouped_matmul_f32": ([P, P, I, P, I, I, P], None),
@@ -127,6 +128,24 @@ def dispatch(x, dst, k: int, m_pad: int) -> np.ndarray:
     D = np.empty((m_pad, H), np.uint16)
     _load().oracle_dispatch(_p(x), T, H, _p(dst), k, m_pad, _p(D))
     return D
+
+
+def combine(Y, dst, w):
+    """Token-ordered staging ``S[t*k+j] = Y[dst[t*k+j]]`` and the combined
+    rows ``C[t] = bf16(sum_j w[t,j] * S[t*k+j])`` (fp32 products and sums in
+    ascending j).  ``Y`` is [rows, N] uint16 bf16 bits, ``dst`` the [T, k]
+    (or flat) destination rows of the dispatch plan, ``w`` [T, k] fp32."""
+    Y = _u16(Y)
+    N = Y.shape[1]
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    T, k = w.shape
+    dst = np.ascontiguousarray(dst, dtype=np.int32).reshape(-1)
+    assert dst.size == T * k
+    assert dst.size == 0 or (dst.min() >= 0 and dst.max() < Y.shape[0])
+    S = np.empty((T * k, N), np.uint16)
+    C = np.empty((T, N), np.uint16)
+    _load().oracle_combine(_p(Y), N, _p(dst), _p(w), T, k, _p(S), _p(C))
+    return S, C
 
 
 def copy_perm(src, perm) -> np.ndarray:

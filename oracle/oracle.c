@@ -20,6 +20,9 @@
  *   gather        G[s*R + i, :] = X_s[i, :]
  *   dispatch      D[dst(t,j), :] = x[t, :], every other row zero
  *   copy_perm     dst[perm[i], :] = src[i, :]
+ *   combine       S[t*k + j, :] = Y[dst(t,j), :]  (token-ordered staging) and
+ *                 C[t, :] = bf16( sum_{j=0..k-1} w[t,j] * f32(S[t*k + j, :]) ),
+ *                 each product and each sum rounded to fp32 in ascending j
  *   matmul_f32    O[m,n] = sum_{k=0..K-1} f32(A[m,k]) * f32(W[k,n]),
  *                 accumulated in fp32 in ascending k (the accumulate precision
  *                 the method fixes: bf16 inputs, fp32 accumulation)
@@ -124,6 +127,35 @@ void oracle_dispatch(const uint16_t *x, int T, int H, const int32_t *dst, int k,
             int64_t r = dst[(int64_t)t * k + j];
             for (int h = 0; h < H; ++h)
                 D[r * H + h] = x[(int64_t)t * H + h];
+        }
+}
+
+/* Combine, the reverse of dispatch ([P1 section 3]: the "layer1 combine"
+ * pushes every expert-output row back to its token's staging row, counted
+ * and published per chunk by the elected last writer).  Pair (t, j) was
+ * dispatched to row dst[t*k + j] of the expert layout; its output row comes
+ * back to staging row t*k + j.  The combined token row is the gate-weighted
+ * sum of its k staged rows.  Reading where the pages are silent: weights are
+ * fp32, the sum runs over j in ascending order with every product and every
+ * partial sum rounded to fp32 (no fused multiply-add), and the result is
+ * rounded to bf16, nearest even. */
+void oracle_combine(const uint16_t *Y, int N, const int32_t *dst, const float *w, int T, int k,
+                    uint16_t *S, uint16_t *C)
+{
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int64_t s = (int64_t)t * k + j;
+            memcpy(S + s * N, Y + (int64_t)dst[s] * N, (size_t)N * sizeof(uint16_t));
+        }
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int64_t s = (int64_t)t * k + j;
+                float prod = w[s] * bf16_to_f32(S[s * N + n]);
+                acc = acc + prod;
+            }
+            C[(int64_t)t * N + n] = f32_to_bf16_rne(acc);
         }
 }
 

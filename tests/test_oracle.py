@@ -295,3 +295,74 @@ def test_ctrl_closed_form_matches_protocol_simulation():
     slot, cnt = _simulate_protocol(4, 128 - p.pad, 128, rng)
     _, _, o_rb = oracle.ctrl_state(4, 0, p.n_blocks)
     assert np.array_equal(o_rb, cnt)
+
+
+# ------------------------------------------------------------------ combine
+def _plan_dst(topk, E):
+    return oracle.dispatch_plan(topk, E).dst.reshape(topk.shape)
+
+
+@pytest.mark.parametrize("routing", ["uniform", "zipf", "one"])
+def test_combine_staging_inverts_dispatch(routing):
+    T, k, E, H = 50, 3, 6, 24
+    topk = {"uniform": lambda: workloads.uniform_topk(T, k, E, 3),
+            "zipf": lambda: workloads.zipf_topk(T, k, E, 1.2, 3),
+            "one": lambda: workloads.all_to_one_topk(T, E, 2)}[routing]()
+    k = topk.shape[1]
+    p = oracle.dispatch_plan(topk, E)
+    x = np.random.default_rng(5).integers(0, 1 << 15, size=(T, H), dtype=np.uint16)
+    D = oracle.dispatch(x, p.dst, k, p.m_pad)
+    S, _ = oracle.combine(D, p.dst, np.ones((T, k), np.float32))
+    # every pair's staged row is its own token's row: dispatch followed by the
+    # combine scatter is the identity on each of the k copies
+    assert np.array_equal(S, np.repeat(x, k, axis=0))
+
+
+def test_combine_single_choice_unit_weight_is_a_gather():
+    rng = np.random.default_rng(7)
+    Y = rng.integers(0, 0x7F00, size=(40, 16), dtype=np.uint16)
+    dst = rng.permutation(40)[:25].astype(np.int32).reshape(25, 1)
+    S, C = oracle.combine(Y, dst, np.ones((25, 1), np.float32))
+    assert np.array_equal(S, Y[dst[:, 0]])
+    assert np.array_equal(C, Y[dst[:, 0]])
+
+
+def test_combine_hand_worked_exact_sums():
+    # rows hold small integers, weights are powers of two: every product and
+    # sum is exact, so C = sum_j w_j * Y[dst_j] can be written out by hand
+    Y = _bf16_bits_from_f32(np.array([[1, 2, 3, 4], [8, 8, 8, 8], [-2, 0, 2, 6]], np.float32))
+    dst = np.array([[1, 0], [2, 2]], np.int32)
+    w = np.array([[0.5, 0.25], [1.0, 0.125]], np.float32)
+    S, C = oracle.combine(Y, dst, w)
+    want = np.array([[4.25, 4.5, 4.75, 5.0], [-2.25, 0.0, 2.25, 6.75]], np.float32)
+    assert np.array_equal(C, _bf16_bits_from_f32(want))
+    assert np.array_equal(S, Y[[1, 0, 2, 2]])
+
+
+def test_combine_rounds_each_product_then_each_sum():
+    # j=0 adds -(1 + 2^-7); j=1 multiplies (1 + 2^-23) by (1 + 2^-7) = 1 + 2^-7
+    # + 2^-23 + 2^-30, which fp32 rounds to 1 + 2^-7 + 2^-23 before the add:
+    # the sum is 2^-23.  A fused multiply-add would keep 2^-30 and give
+    # 2^-23 * (1 + 2^-7), which bf16 represents, so the two readings differ.
+    a = np.float32(1 + 2.0 ** -7)
+    Y = _bf16_bits_from_f32(np.array([[-a], [a]], np.float32))
+    w = np.array([[1.0, 1 + 2.0 ** -23]], np.float32)
+    assert w[0, 1] != 1.0
+    _, C = oracle.combine(Y, np.array([[0, 1]], np.int32), w)
+    assert _f64_from_bits(C)[0, 0] == 2.0 ** -23
+
+
+def test_combine_within_fp32_bound_of_float64():
+    rng = np.random.default_rng(11)
+    T, k, N, rows = 64, 4, 48, 300
+    Y = _bf16_bits_from_f32(rng.standard_normal((rows, N)).astype(np.float32))
+    dst = rng.integers(0, rows, size=(T, k)).astype(np.int32)
+    logits = rng.standard_normal((T, k))
+    w = (np.exp(logits) / np.exp(logits).sum(1, keepdims=True)).astype(np.float32)
+    _, C = oracle.combine(Y, dst, w)
+    Yf = _f64_from_bits(Y)
+    exact = np.einsum("tj,tjn->tn", w.astype(np.float64), Yf[dst])
+    mag = np.einsum("tj,tjn->tn", np.abs(w.astype(np.float64)), np.abs(Yf[dst]))
+    got = _f64_from_bits(C)
+    bound = 2 * k * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(exact) + 1e-30
+    assert np.all(np.abs(got - exact) <= bound)
