@@ -377,14 +377,38 @@ def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int):
         timer = Timer(stream)
         fn = lambda: h.dispatch_grouped_gemm(x, topk, W, dispatched, offs, out)  # noqa: E731
         timer.time_calls(fn, 3)
-        ms = statistics.median(timer.time_calls(fn, rounds))
+        ms = statistics.mean(timer.time_calls(fn, rounds))
         assert h.sync_status() == 0
         counts = np.bincount(topk_np.reshape(-1), minlength=cfg.E)
         m_pad = int(offs[-1].item())
         flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.N
-        return {"workload": cfg.name, "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
-                "algorithmic_GFLOP": flops / 1e9, "padded_rows": m_pad, "max_expert_rows": int(counts.max()),
-                "min_expert_rows": int(counts.min()), "rounds": rounds, "l2": "flushed before every round"}
+        res = {"workload": cfg.name, "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+               "algorithmic_GFLOP": flops / 1e9, "padded_rows": m_pad, "max_expert_rows": int(counts.max()),
+               "min_expert_rows": int(counts.min()), "rounds": rounds, "l2": "flushed before every round"}
+        res["combine"] = combine_bench(h, cfg, out, timer, rounds, dev)
+        return res
+
+
+def combine_bench(h, cfg, y, timer, rounds: int, dev):
+    """Combine of the dispatch round just run on `h`: algorithmic bytes =
+    expert rows read + staging written + staging read + combined written
+    (+ weights), per call, against the measured HBM copy bandwidth."""
+    import torch
+    import workloads
+    T, k, N = cfg.T, cfg.k, cfg.N
+    w = torch.from_numpy(workloads.gate_weights(T, k, 0)).to(dev)
+    staging = torch.empty(T * k, N, dtype=torch.bfloat16, device=dev)
+    combined = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+    fn = lambda: h.combine(y, w, staging, combined)  # noqa: E731
+    timer.time_calls(fn, 3)
+    ms = statistics.mean(timer.time_calls(fn, rounds))
+    assert h.sync_status() == 0
+    nbytes = 3.0 * T * k * N * 2 + T * N * 2 + T * k * 4
+    peaks, _ = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms_per_round": ms, "GB/s": gbs, "algorithmic_MB": nbytes / 1e6, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "producer_ctas": h.get_option(1), "reducer_ctas": h.get_option(2),
+            "l2": "flushed before every call (expert outputs start in HBM)"}
 
 
 def copy_sweep(rounds: int, dev, sizes):

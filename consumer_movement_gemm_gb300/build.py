@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtovl.so")
-SOURCES = ["tovl_api.cu", "fused.cu", "plan.cu", "copy.cu", "plan_static.cu"]
+SOURCES = ["tovl_api.cu", "fused.cu", "plan.cu", "copy.cu", "plan_static.cu", "combine.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

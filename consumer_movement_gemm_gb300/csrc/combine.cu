@@ -1,0 +1,49 @@
+// combine.cu -- the combine kernel: producer CTAs stage expert-output rows in
+// token order with per-chunk watermarks, reducer CTAs wait on the watermarks
+// and write the gate-weighted sums.  One persistent grid, every CTA resident
+// (cooperative launch), so a reducer's wait always has a live producer.
+#include "combine.cuh"
+#include "launch.cuh"
+#include "producer.cuh"
+
+namespace tovl {
+
+__global__ void __launch_bounds__(kThreads, 1) combine_kernel(const __grid_constant__ FusedParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    if (static_cast<int>(blockIdx.x) < p.n_producers) producer(p, smem, blockIdx.x);
+    else reducer(p, blockIdx.x - p.n_producers);
+}
+
+// Shared memory: the staged producer path keeps one 8 KB buffer and one
+// mbarrier per warp; the vector path needs none, which leaves the SM's whole
+// L1 to the copies.
+static int combine_smem(int producer_mode)
+{
+    return producer_mode == 1 ? (kThreads / 32) * (kItemBytes + 8) + 1024 : 0;
+}
+
+cudaError_t prepare_combine()
+{
+    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem(1));
+}
+
+cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative)
+{
+    const int grid = p.n_producers + p.n_reducers;
+    if (grid <= 0) return cudaSuccess;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = combine_smem(p.producer_mode);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = cooperative ? 1 : 0;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, combine_kernel, p);
+}
+
+}  // namespace tovl

@@ -1,0 +1,71 @@
+// combine.cuh -- reducer CTAs of the combine kernel.
+//
+// Combine is dispatch in reverse ("cross-GPU sync protocols on PCIe",
+// section 3: the layer-1 combine pushes each expert-output row back to its
+// token's staging row and the last writer of a chunk, elected by an acq_rel
+// count, publishes the chunk's slot).  The producer CTAs of the combine
+// kernel are the fused kernel's producers with a row table: staging row
+// t*k + j copies expert-output row dst(t, j).  The reducers below wait for
+// the slots of the chunks that hold a token's k staged rows (acquire polls
+// of local slots, warp vote) and write the token's combined row
+//   combined[t, :] = bf16( sum_j w[t*k + j] * staging[t*k + j, :] ),
+// every product and every partial sum rounded to fp32, j ascending.
+#pragma once
+#include "common.cuh"
+#include "ctrl.cuh"
+#include "ptx.cuh"
+#include "sync.cuh"
+
+namespace tovl {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ inline void reducer(const FusedParams& p, int rid)
+{
+    const int warp = threadIdx.x / 32;
+    const int lane = static_cast<int>(ptx::lane_id());
+    if (gather_rows(p) == 0) {
+        // the routing plan of the round was rejected: nothing to combine
+        if (rid == 0 && threadIdx.x == 0) record_error(p.ctrl, kErrInvalid);
+        return;
+    }
+    // consecutive tokens go to different CTAs, in the producers' order
+    const int gw = warp * p.n_reducers + rid;
+    const int n_gw = p.n_reducers * (kThreads / 32);
+    const int S = p.ctrl.n_slices;
+    const int groups = p.N / 8;   // 16-byte column groups of a row
+    const size_t row_bytes = static_cast<size_t>(p.N) * 2;
+    const uint8_t* staging = static_cast<const uint8_t*>(p.gathered);
+    uint8_t* out = static_cast<uint8_t*>(p.combined);
+    for (int t = gw; t < p.T; t += n_gw) {
+        const int s0 = t * p.k;
+        const int c0 = s0 / kChunkRows, c1 = (s0 + p.k - 1) / kChunkRows;
+        const int* words[2] = {p.ctrl.slot + c0 * S, p.ctrl.slot + c1 * S};
+        if (warp_wait_ge(words, c1 != c0 ? 2 : 1, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
+        for (int g = lane; g < groups; g += 32) {
+            float acc[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+            for (int j = 0; j < p.k; ++j) {
+                const float w = p.gate_w[s0 + j];
+                const int4 v = ptx::ld_v4(reinterpret_cast<const int4*>(staging + (s0 + j) * row_bytes) + g);
+                const uint32_t u[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
+                                       static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(w, bf16_lo(u[c])));
+                    acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(w, bf16_hi(u[c])));
+                }
+            }
+            int4 o;
+            o.x = static_cast<int>(ptx::pack_bf16x2(acc[0], acc[1]));
+            o.y = static_cast<int>(ptx::pack_bf16x2(acc[2], acc[3]));
+            o.z = static_cast<int>(ptx::pack_bf16x2(acc[4], acc[5]));
+            o.w = static_cast<int>(ptx::pack_bf16x2(acc[6], acc[7]));
+            ptx::st_v4(reinterpret_cast<int4*>(out + static_cast<size_t>(t) * row_bytes) + g, o);
+        }
+    }
+}
+
+}  // namespace tovl

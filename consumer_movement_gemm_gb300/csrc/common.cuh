@@ -28,9 +28,16 @@ __device__ __forceinline__ void trace_put(const FusedParams& p, long long idx, u
 }
 
 // Number of 128-row blocks the producers fill and the consumers traverse.
+// Rows of a gather-mode round: p.M, or none when the round's row table comes
+// from a routing plan that was rejected.
+__device__ __forceinline__ int gather_rows(const FusedParams& p)
+{
+    return (p.rows_valid && p.rows_valid[1] <= 0) ? 0 : p.M;
+}
+
 __device__ __forceinline__ int num_row_blocks(const FusedParams& p)
 {
-    if (p.mode == kModeGather) return (p.M + kTileM - 1) / kTileM;
+    if (p.mode == kModeGather) return (gather_rows(p) + kTileM - 1) / kTileM;
     return p.meta[1];
 }
 

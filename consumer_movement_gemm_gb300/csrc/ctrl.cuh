@@ -137,6 +137,13 @@ struct FusedParams {
     const int* pad;
     const int* blk_expert;
     const int* meta;
+    // combine sources (gather mode with a row table)
+    const int* src_rows;  // non-null: destination row r copies row src_rows[r] of x
+    const int* rows_valid;  // non-null: the round has rows only if rows_valid[1] > 0 (plan block count)
+    const float* gate_w;  // [T*k] combine weights
+    void* combined;       // [T][N] bf16 combined rows
+    int n_reducers;
+    int T, k;
     // destinations
     void* gathered;       // gathered / dispatched buffer
     void* out;            // [rows][N] bf16

@@ -10,6 +10,9 @@ cudaError_t prepare_fused();
 int fused_max_active_per_sm();
 int fused_max_active_pairs();
 
+cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative);
+cudaError_t prepare_combine();
+
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t prepare_plan();
 

@@ -42,7 +42,8 @@ __device__ __forceinline__ Item decode_item(const FusedParams& p, int i, int n_b
 __device__ __forceinline__ const uint8_t* row_src(const FusedParams& p, int r)
 {
     if (p.mode == kModeGather) {
-        if (r >= p.M) return nullptr;
+        if (r >= gather_rows(p)) return nullptr;
+        if (p.src_rows) return static_cast<const uint8_t*>(p.x) + static_cast<size_t>(p.src_rows[r]) * p.row_bytes;
         const int s = r / p.rows_per_shard;
         const int i = r - s * p.rows_per_shard;
         return static_cast<const uint8_t*>(p.shard[s]) + static_cast<size_t>(i) * p.row_bytes;
@@ -72,7 +73,7 @@ __device__ __forceinline__ void item_done(const FusedParams& p, int counter, int
 // does not use at all (chunks past the rows, slices past k_slices, the other
 // counter family) -- only keep the closed form, so they are added after the
 // copies, off the consumers' critical path.
-__device__ void seed_counters(const FusedParams& p, int gw, int n_gw, bool completion)
+__device__ inline void seed_counters(const FusedParams& p, int gw, int n_gw, bool completion)
 {
     const uint32_t lane = ptx::lane_id();
     const Ctrl& c = p.ctrl;
@@ -81,7 +82,7 @@ __device__ void seed_counters(const FusedParams& p, int gw, int n_gw, bool compl
     for (int cs = gw * 32 + lane; cs < c.n_chunk_cap * S; cs += n_gw * 32) {
         const int ch = cs / S, sl = cs - ch * S;
         int real = 0;
-        if (p.mode == kModeGather && sl < p.k_slices) real = min(max(p.M - ch * kChunkRows, 0), kChunkRows);
+        if (p.mode == kModeGather && sl < p.k_slices) real = min(max(gather_rows(p) - ch * kChunkRows, 0), kChunkRows);
         const bool is_completion = real > 0 && real < kChunkRows;
         if (is_completion == completion && real < kChunkRows) arrive_and_publish(c, cs, kChunkRows - real, p.seq);
     }
@@ -156,7 +157,10 @@ template <int M>
 __device__ __forceinline__ ItemState<M> begin_item(const FusedParams& p, const LaneMap<M>& lm, int i, int n_blocks)
 {
     const int lane = static_cast<int>(ptx::lane_id());
-    const uint8_t* dummy = static_cast<const uint8_t*>(p.mode == kModeGather ? p.shard[0] : p.x);
+    // a readable row for lanes whose row has no source: the shards' first
+    // row for an all-gather, the source buffer for a row table or a dispatch
+    const uint8_t* dummy =
+        static_cast<const uint8_t*>((p.mode == kModeGather && !p.src_rows) ? p.shard[0] : p.x);
     ItemState<M> st;
     st.it = decode_item(p, i, n_blocks);
     const size_t soff = static_cast<size_t>(kb_begin(p, st.it.s)) * kTileK * 2;
@@ -305,7 +309,7 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
     }
 }
 
-__device__ void producer(const FusedParams& p, uint8_t* smem, int pid)
+__device__ inline void producer(const FusedParams& p, uint8_t* smem, int pid)
 {
     const int warp = threadIdx.x / 32;
     const int n_warps = kThreads / 32;

@@ -135,6 +135,19 @@ __device__ __forceinline__ int4 ld_nc_v4(const int4* p)
     return v;
 }
 
+// Plain (weak) 16-byte load, for data another CTA wrote during this launch
+// and published through the protocol (the non-coherent path is for data
+// that is read-only for the whole launch).
+__device__ __forceinline__ int4 ld_v4(const int4* p)
+{
+    int4 v;
+    asm volatile("ld.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(int4* p, int4 v)
 {
     asm volatile("st.global.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

@@ -217,6 +217,7 @@ TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
         if ((e = prepare_fused()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare fused"); break; }
         if ((e = prepare_plan()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare plan"); break; }
         if ((e = prepare_copy()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare copy"); break; }
+        if ((e = prepare_combine()) != cudaSuccess) { rc = cuda_fail(h, e, "prepare combine"); break; }
         if (fused_max_active_per_sm() < 1) { rc = TOVL_ERR_UNSUPPORTED; break; }
         h->max_pairs = fused_max_active_pairs();
 
@@ -599,6 +600,70 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     h->last_T = T;
     h->last_k = k;
     h->last_E = E;
+    return TOVL_OK;
+}
+
+TOVL_API int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void* staging, void* combined,
+                          void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (h->last_T <= 0 && h->last_k <= 0) return TOVL_ERR_INVALID;   // no dispatch round on this handle yet
+    if (!y || !gate_w || !staging || !combined) return TOVL_ERR_INVALID;
+    if (!aligned16(y) || !aligned16(staging) || !aligned16(combined) || (reinterpret_cast<uintptr_t>(gate_w) & 3u))
+        return TOVL_ERR_INVALID;
+    if (N < kTileK || N % kTileK) return TOVL_ERR_INVALID;
+    if (N > kMaxK) return TOVL_ERR_UNSUPPORTED;
+    const long long pairs = static_cast<long long>(h->last_T) * h->last_k;
+    if (pairs > h->cfg.max_rows) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FusedParams p;
+    base_params(h, p);
+    p.mode = kModeGather;
+    p.M = static_cast<int>(pairs);     // staging rows, token-major: row t*k + j
+    p.N = N;
+    p.K = N;
+    p.n_kb = N / kTileK;
+    p.n_nb = 0;
+    p.row_bytes = N * 2;
+    // copy traffic 2 x rows x N x 2 bytes against the reduction's k+1 rows
+    // per token: about half the SMs copy, the rest reduce
+    int P = h->producers > 0 ? h->producers : h->num_sms / 2;
+    if (P > h->num_sms - 1) P = h->num_sms - 1;
+    p.n_producers = P;
+    p.n_reducers = h->num_sms - P;
+    h->last_P = P;
+    h->last_C = p.n_reducers;
+    p.k_slices = 1;
+    {
+        const int n16 = p.n_kb * kTileK * 2 / 16;
+        int ri = 64;
+        while (ri > 1 && ri * n16 > kItemInt4) ri >>= 1;
+        p.item_rows = ri;
+    }
+    p.wave_blocks = static_cast<int>(ceil_div(pairs, kBlockRows));   // one ordering group: token order
+    if (p.wave_blocks < 1) p.wave_blocks = 1;
+    p.x = y;
+    p.src_rows = h->plan.dst;
+    p.rows_valid = h->plan.meta;
+    p.gate_w = gate_w;
+    p.gathered = staging;
+    p.combined = combined;
+    p.T = h->last_T;
+    p.k = h->last_k;
+    p.seq = static_cast<int>(h->seq + 1);
+    p.gate_seq = p.seq + h->fault_gate_offset;
+    p.trace_tiles = 0;
+    int rc;
+    if ((rc = reset_stats(h, s, 0, 1)) != TOVL_OK) return rc;
+    cudaError_t e = launch_combine(p, s, h->coop_enabled);
+    if (e != cudaSuccess && h->coop_enabled) {
+        cudaGetLastError();
+        e = launch_combine(p, s, false);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->seq += 1;
+    h->last_stream = s;
     return TOVL_OK;
 }
 

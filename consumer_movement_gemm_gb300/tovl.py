@@ -79,6 +79,7 @@ SIGNATURES = {
     "tovl_gather_gemm": ([_P, ctypes.POINTER(_P), _I, _I, _I, _P, _I, _P, _P, _P], _I),
     "tovl_dispatch_rows": ([_I, _I, _I], _LL),
     "tovl_dispatch_grouped_gemm": ([_P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _P, _P], _I),
+    "tovl_combine": ([_P, _P, _I, _P, _P, _P, _P], _I),
     "tovl_gemm_only": ([_P, _P, _I, _I, _P, _I, _P, _P], _I),
     "tovl_copy_only": ([_P, ctypes.POINTER(_P), _I, _I, _I, _P, _P], _I),
     "tovl_gated_copy": ([_P, _P, _P, _LL, _I, _P, _I, _I, _P], _I),
@@ -220,6 +221,16 @@ class Handle:
         ptrs, S, R, K = _shard_ptrs(shards)
         rc = load().tovl_copy_only(self.h, ptrs, S, R, K, _ptr(gathered), _stream(stream))
         _check(self.h, rc, "tovl_copy_only")
+
+    def combine(self, y, gate_w, staging, combined, stream=None):
+        """Combine of the last dispatch round: ``staging[t*k+j] = y[dst(t,j)]``
+        and ``combined[t] = bf16(sum_j gate_w[t,j] * staging[t*k+j])``."""
+        N = y.shape[1]
+        import torch
+        if gate_w.dtype != torch.float32:
+            raise TypeError("gate weights must be float32")
+        rc = load().tovl_combine(self.h, _ptr(y), N, _ptr(gate_w), _ptr(staging), _ptr(combined), _stream(stream))
+        _check(self.h, rc, "tovl_combine")
 
     def gated_copy(self, src, dst, perm, gated=True, stamps=False, stream=None):
         n, rb = src.shape

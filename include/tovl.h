@@ -135,6 +135,29 @@ int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const
                                const void* W, int N, void* dispatched, int* expert_offsets, void* out,
                                void* stream);
 
+/* Combine: the reverse of the last dispatch round on this handle ("cross-GPU
+ * sync protocols on PCIe", section 3, the layer-1 combine: every expert
+ * output row goes back to its token's staging row; each 64-row staging chunk
+ * is counted with acq_rel atomics and published by the elected last writer;
+ * reducers poll the chunk slots with acquire loads).
+ *   y           device, bf16 [rows][N]: expert outputs in the dispatched layout
+ *               of the last tovl_dispatch_grouped_gemm call (its `out`)
+ *   N           row length of y, multiple of 64, at most 32768
+ *   gate_w      device, fp32 [T][k]: weight of pair (t, j)
+ *   staging     device, bf16 [T*k][N]: receives staging[t*k + j] = y[dst(t, j)]
+ *   combined    device, bf16 [T][N]: receives round-to-nearest-even of
+ *               sum_j gate_w[t][j] * staging[t*k + j], every product and every
+ *               partial sum rounded to fp32, j ascending
+ *   stream      cudaStream_t, ordered after the dispatch call
+ * T, k and the routing plan are the last dispatch call's; T*k <= max_rows.
+ * Without an earlier dispatch on the handle the call returns
+ * TOVL_ERR_INVALID; after a dispatch whose plan was rejected (bad expert id)
+ * the round is a no-op that sets TOVL_ERR_INVALID in the status word.  One
+ * round (one sequence number), like the other calls.  Option 1 (producer
+ * CTAs) applies; the remaining SMs reduce (default: half and half). */
+int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void* staging, void* combined,
+                 void* stream);
+
 /* ---------------------------------------------------------------- no-allocation plan
  * The pages have no counterpart to this entry point; it serves callers that
  * must not allocate device memory themselves (code inside another

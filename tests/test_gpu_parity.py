@@ -233,6 +233,108 @@ def test_dispatch_bad_expert_id_is_a_noop_round():
         _check_dispatch(h, x, topk_np, W, dispatched, offs, out, 2)
 
 
+# ------------------------------------------------------------------ combine
+def _combine_round(h, rows, N, T, k, seed):
+    y = workloads.bf16_normal((rows, N), 1.0, seed, DEV)
+    w_np = workloads.gate_weights(T, k, seed + 1)
+    w = torch.from_numpy(w_np).to(DEV)
+    staging = torch.full((max(T * k, 1), N), 5.0, dtype=torch.bfloat16, device=DEV)
+    combined = torch.full((max(T, 1), N), 5.0, dtype=torch.bfloat16, device=DEV)
+    h.combine(y, w, staging, combined)
+    return y, w_np, staging, combined
+
+
+@pytest.mark.parametrize("routing", list(ROUTINGS))
+@pytest.mark.parametrize("mode", [0, 1])
+def test_combine_after_dispatch(routing, mode):
+    # combine runs on a seeded expert-output tensor, so staging and combined
+    # rows are compared bit for bit with the oracle's
+    H, N = 128, 320
+    with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_PRODUCER_MODE, mode)
+        R = 0
+        for r in range(1, 4):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(2, r))
+            T, k = topk_np.shape
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 400 + r, DEV)
+            W = workloads.bf16_normal((E, H, 256), 1 / math.sqrt(H), 500 + r, DEV)
+            _dispatch_round(h, x, topk_np, W)
+            R += 1
+            rows = tovl.dispatch_rows(T, k, E)
+            y, w_np, staging, combined = _combine_round(h, rows, N, T, k, 600 + r)
+            R += 1
+            assert h.sync_status() == 0
+            p = oracle.dispatch_plan(topk_np, E)
+            S, C = oracle.combine(bits(y), p.dst, w_np)
+            assert np.array_equal(bits(staging[:T * k]), S), "staging"
+            assert np.array_equal(bits(combined[:T]), C), "combined"
+            _check_ctrl(h, R)
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (21, 3, 5), (64, 1, 2), (100, 8, 16)])
+def test_combine_shapes(T, k, E):
+    # one token; tokens straddling 64-row chunks (k=3); exactly one chunk;
+    # k=8 with a ragged last chunk
+    H, N = 64, 64
+    with _handle() as h:
+        topk_np = workloads.uniform_topk(T, k, E, 9)
+        x = workloads.bf16_normal((T, H), 1.0, 1, DEV)
+        W = workloads.bf16_normal((E, H, 256), 1.0, 2, DEV)
+        _dispatch_round(h, x, topk_np, W)
+        y, w_np, staging, combined = _combine_round(h, tovl.dispatch_rows(T, k, E), N, T, k, 3)
+        assert h.sync_status() == 0
+        S, C = oracle.combine(bits(y), oracle.dispatch_plan(topk_np, E).dst, w_np)
+        assert np.array_equal(bits(staging[:T * k]), S)
+        assert np.array_equal(bits(combined[:T]), C)
+        _check_ctrl(h, 2)
+
+
+def test_moe_layer_dispatch_gemm_combine():
+    # the whole layer against the oracle's: dispatch, grouped GEMM, combine
+    T, H, k, E, N = 300, 256, 2, 6, 512
+    with _handle() as h:
+        topk_np = workloads.uniform_topk(T, k, E, 21)
+        x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 22, DEV)
+        W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 23, DEV)
+        dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+        w_np = workloads.gate_weights(T, k, 24)
+        staging = torch.empty(T * k, N, dtype=torch.bfloat16, device=DEV)
+        combined = torch.empty(T, N, dtype=torch.bfloat16, device=DEV)
+        h.combine(out, torch.from_numpy(w_np).to(DEV), staging, combined)
+        assert h.sync_status() == 0
+        p = oracle.dispatch_plan(topk_np, E)
+        D = oracle.dispatch(bits(x), p.dst, k, p.m_pad)
+        Y = oracle.f32_to_bf16(oracle.grouped_matmul_f32(D, bits(W), p.off))
+        _, C = oracle.combine(Y, p.dst, w_np)
+        assert_close(combined, oracle.bf16_to_f32(C), "combined layer")
+        _check_ctrl(h, 2)
+
+
+def test_combine_timeout_and_rejected_plan():
+    H, N = 64, 64
+    with _handle(wait_timeout_ns=5_000_000) as h:
+        topk_np = workloads.uniform_topk(50, 2, 4, 5)
+        x = workloads.bf16_normal((50, H), 1.0, 1, DEV)
+        W = workloads.bf16_normal((4, H, 256), 1.0, 2, DEV)
+        _dispatch_round(h, x, topk_np, W)
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # reducers wait for a sequence nobody publishes
+        _combine_round(h, tovl.dispatch_rows(50, 2, 4), N, 50, 2, 3)
+        assert h.sync_status() == tovl.TOVL_ERR_TIMEOUT
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 0)
+        y, w_np, staging, combined = _combine_round(h, tovl.dispatch_rows(50, 2, 4), N, 50, 2, 4)
+        assert h.sync_status() == 0
+        S, C = oracle.combine(bits(y), oracle.dispatch_plan(topk_np, 4).dst, w_np)
+        assert np.array_equal(bits(combined[:50]), C)
+        _check_ctrl(h, 3)
+        # a rejected plan makes the next combine a no-op round that reports it
+        bad = np.array([[0, 1], [2, 9]], np.int32)
+        _dispatch_round(h, x[:2], bad, W)
+        assert h.sync_status() == tovl.TOVL_ERR_INVALID
+        _combine_round(h, 256, N, 2, 2, 5)
+        assert h.sync_status() == tovl.TOVL_ERR_INVALID
+        _check_ctrl(h, 5)
+
+
 # ------------------------------------------------------------------ gated copy
 @pytest.mark.parametrize("row_bytes", [256, 1024, 8192])
 @pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK])

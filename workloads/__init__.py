@@ -149,6 +149,15 @@ def routing(cfg: DispatchCfg, seed: int) -> np.ndarray:
     raise ValueError(cfg.routing)
 
 
+def gate_weights(T: int, k: int, seed: int) -> np.ndarray:
+    """Router gate weights of the k chosen experts: softmax of N(0,1) logits
+    over each token's k choices (fp32 [T][k], rows sum to 1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    z = rng.standard_normal((T, k))
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
 def all_to_one_topk(T: int, E: int, e: int = 0) -> np.ndarray:
     """Degenerate routing: every token to expert e (k = 1)."""
     return np.full((T, 1), e, np.int32)
