@@ -12,6 +12,8 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const __grid_const
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
+    // the expert outputs and the plan come from the kernels before this one
+    ptx::grid_dep_wait();
     if (static_cast<int>(blockIdx.x) < p.n_producers) producer(p, smem, blockIdx.x);
     else reducer(p, blockIdx.x - p.n_producers);
 }
@@ -29,7 +31,7 @@ cudaError_t prepare_combine()
     return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem(1));
 }
 
-cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative)
+cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative, bool pdl)
 {
     const int grid = p.n_producers + p.n_reducers;
     if (grid <= 0) return cudaSuccess;
@@ -38,11 +40,13 @@ cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool coope
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = combine_smem(p.producer_mode);
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = cooperative ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&lc, combine_kernel, p);
 }
 

@@ -408,7 +408,6 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     using T = Tile<PAIR>;
     const int warp = threadIdx.x / 32;
     const ConsumerSmem<PAIR> s = consumer_smem<PAIR>(smem);
-    const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
     if (threadIdx.x == 0) {
         for (int i = 0; i < T::kStages; ++i) {
             ptx::mbar_init(&s.full[i], 1);
@@ -441,6 +440,10 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     else ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
+    // the prologue above overlaps the previous kernel; the schedule (a
+    // dispatch plan's block count), the gates and the operands are its output
+    ptx::grid_dep_wait();
+    const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
 
     if (warp == 0) consumer_tma<PAIR>(p, s, sc);
     else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);

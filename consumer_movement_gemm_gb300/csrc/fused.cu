@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     else consumer<PAIR>(p, smem, blockIdx.x - p.n_producers);
 }
 
-cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair)
+cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair, bool pdl)
 {
     const int grid = p.n_producers + p.n_consumers;
     if (grid <= 0) return cudaSuccess;
@@ -49,11 +49,18 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = smem_bytes(pair);
     lc.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int n = 0;
     attr[n].id = cudaLaunchAttributeCooperative;
     attr[n].val.cooperative = cooperative ? 1 : 0;
     ++n;
+    if (pdl) {
+        // the kernel's prologue may overlap the previous kernel's tail; every
+        // role waits (griddepcontrol.wait) before it reads global memory
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     if (pair == 2) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = 2;

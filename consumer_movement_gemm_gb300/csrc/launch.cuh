@@ -5,15 +5,15 @@
 
 namespace tovl {
 
-cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair);
+cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair, bool pdl);
 cudaError_t prepare_fused();
 int fused_max_active_per_sm();
 int fused_max_active_pairs();
 
-cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative);
+cudaError_t launch_combine(const FusedParams& p, cudaStream_t stream, bool cooperative, bool pdl);
 cudaError_t prepare_combine();
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream, bool pdl);
 cudaError_t prepare_plan();
 
 cudaError_t launch_copy(const CopyParams& p, int n_waiters, cudaStream_t stream);

@@ -28,6 +28,7 @@ constexpr int kPlanWarps = kPlanThreads / 32;
 __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const PlanParams p)
 {
     extern __shared__ int wcnt[];               // [kPlanWarps][E]
+    ptx::grid_dep_launch();                     // the finalize kernel may start its launch
     const int tid = threadIdx.x;
     const int warp = tid / 32;
     const int lane = tid % 32;
@@ -69,6 +70,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
     int* s_cnt = sm + p.E + 1;      // [E]
     __shared__ int s_zero;
     __shared__ int s_bad;
+    // the counting grid (launched just before, programmatically) has finished
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();         // the fused kernel may start its launch and prologue
     const int tid = threadIdx.x;
     const int* meta_in = p.plan.meta;
     if (tid == 0) {
@@ -149,7 +153,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
 
 namespace tovl {
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream)
+// The finalize kernel is launched with a programmatic edge on the counting
+// grid when `pdl` is set (it waits for the counts with griddepcontrol.wait).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream, bool pdl)
 {
     const size_t sm_count = static_cast<size_t>(kPlanWarps) * p.E * sizeof(int);
     const size_t sm_fin = static_cast<size_t>(2 * p.E + 1) * sizeof(int);
@@ -158,8 +164,17 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream)
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    plan_finalize_kernel<<<1, kPlanThreads, sm_fin, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(kPlanThreads);
+    lc.dynamicSmemBytes = sm_fin;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = (pdl && p.n_seg > 0) ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, plan_finalize_kernel, p);
 }
 
 cudaError_t prepare_plan()

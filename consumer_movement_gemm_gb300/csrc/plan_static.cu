@@ -108,5 +108,5 @@ TOVL_API int tovl_dispatch_plan_noalloc(const int* topk_idx, int T, int k, int E
     // The array keeps the previous call's contents; the routing-error flag in
     // meta must start at zero (every other piece is overwritten before use).
     if (cudaMemsetAsync(base + kOffMeta, 0, 4 * sizeof(int), s) != cudaSuccess) return TOVL_ERR_CUDA;
-    return launch_plan(pp, s) == cudaSuccess ? TOVL_OK : TOVL_ERR_CUDA;
+    return launch_plan(pp, s, false) == cudaSuccess ? TOVL_OK : TOVL_ERR_CUDA;
 }

@@ -318,6 +318,8 @@ __device__ inline void producer(const FusedParams& p, uint8_t* smem, int pid)
     const int gw = warp * p.n_producers + pid;
     const int n_gw = p.n_producers * n_warps;
     if (threadIdx.x == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
+    // sources, plan and counters were written by earlier kernels
+    ptx::grid_dep_wait();
     seed_counters(p, gw, n_gw, true);
     if (p.producer_mode == 1) {
         if (p.item_rows <= 16) copy_items_staged<1>(p, smem, gw, n_gw);

@@ -154,6 +154,21 @@ __device__ __forceinline__ void st_v4(int4* p, int4 v)
                  : "memory");
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// Wait until the grids this one depends on have completed and their writes
+// are visible (returns at once when the launch had no programmatic edge).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream start launching (it still waits for this
+// grid's completion before it reads anything).
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {

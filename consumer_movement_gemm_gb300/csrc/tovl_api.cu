@@ -42,6 +42,8 @@ struct tovl_ctx {
     bool coop_pairs = true;  // cooperative launch accepted together with clusters
     bool coop_enabled = true;  // fused launches ask for the co-residency guarantee
     int producer_mode = 0;     // fused producers: 0 vector copies, 1 staged bulk loads
+    bool pdl = true;           // programmatic dependent launch between this library's kernels
+    bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
     Ctrl ctrl{};
     Plan plan{};
@@ -366,10 +368,17 @@ static cudaError_t launch(tovl_ctx* h, const FusedParams& p, cudaStream_t s, boo
 {
     if (pair == 2 && !h->coop_pairs) cooperative = false;
     if (!h->coop_enabled) cooperative = false;
-    cudaError_t e = launch_fused(p, s, cooperative, pair);
+    bool pdl = h->pdl && h->pdl_ok;
+    cudaError_t e = launch_fused(p, s, cooperative, pair, pdl);
+    if (e != cudaSuccess && pdl) {
+        cudaGetLastError();
+        pdl = false;
+        e = launch_fused(p, s, cooperative, pair, false);
+        if (e == cudaSuccess) h->pdl_ok = false;
+    }
     if (e != cudaSuccess && pair == 2 && cooperative) {
         cudaGetLastError();
-        e = launch_fused(p, s, false, pair);
+        e = launch_fused(p, s, false, pair, pdl);
         if (e == cudaSuccess) h->coop_pairs = false;
     }
     return e;
@@ -552,7 +561,12 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     pp.expert_offsets = expert_offsets;
     pp.plan = h->plan;
     pp.status = h->ctrl.status;
-    cudaError_t e = launch_plan(pp, s);
+    cudaError_t e = launch_plan(pp, s, h->pdl && h->pdl_ok);
+    if (e != cudaSuccess && h->pdl && h->pdl_ok) {
+        cudaGetLastError();
+        h->pdl_ok = false;
+        e = launch_plan(pp, s, false);
+    }
     if (e != cudaSuccess) return cuda_fail(h, e, "plan launch");
 
     FusedParams p;
@@ -656,10 +670,11 @@ TOVL_API int tovl_combine(tovl_handle h, const void* y, int N, const float* gate
     p.trace_tiles = 0;
     int rc;
     if ((rc = reset_stats(h, s, 0, 1)) != TOVL_OK) return rc;
-    cudaError_t e = launch_combine(p, s, h->coop_enabled);
-    if (e != cudaSuccess && h->coop_enabled) {
+    const bool pdl = h->pdl && h->pdl_ok;
+    cudaError_t e = launch_combine(p, s, h->coop_enabled, pdl);
+    if (e != cudaSuccess && (h->coop_enabled || pdl)) {
         cudaGetLastError();
-        e = launch_combine(p, s, false);
+        e = launch_combine(p, s, false, false);
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
     h->seq += 1;
@@ -876,6 +891,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != 0 && value != 1) return TOVL_ERR_INVALID;
         h->producer_mode = static_cast<int>(value);
         return TOVL_OK;
+    case 15:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->pdl = value != 0;
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -899,6 +918,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 12: *value = h->coop_pairs ? 1 : 0; return TOVL_OK;
     case 13: *value = h->coop_enabled ? 1 : 0; return TOVL_OK;
     case 14: *value = h->producer_mode; return TOVL_OK;
+    case 15: *value = (h->pdl && h->pdl_ok) ? 1 : 0; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

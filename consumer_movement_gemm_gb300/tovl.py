@@ -38,6 +38,7 @@ OPT_MAX_PAIRS = 11
 OPT_COOP_PAIRS = 12
 OPT_COOPERATIVE = 13
 OPT_PRODUCER_MODE = 14
+OPT_PDL = 15
 
 
 class TovlError(RuntimeError):

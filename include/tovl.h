@@ -255,6 +255,11 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * stores through registers (the default), 1 = bulk asynchronous loads of each
  * row segment into a per-warp shared-memory buffer, then 16-byte vector
  * stores (results are identical),
+ * 15 = programmatic dependent launch between the library's own kernels
+ * (1, the default: a kernel's launch and prologue overlap the end of the
+ * kernel before it -- plan counting, plan finalisation, the fused kernel,
+ * combine -- and every kernel waits for its predecessor before it reads
+ * memory; 0 = plain stream order; reads back 0 if the device refused it),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

@@ -245,13 +245,16 @@ def _combine_round(h, rows, N, T, k, seed):
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
-@pytest.mark.parametrize("mode", [0, 1])
-def test_combine_after_dispatch(routing, mode):
+@pytest.mark.parametrize("mode,pdl", [(0, 1), (1, 1), (0, 0)])
+def test_combine_after_dispatch(routing, mode, pdl):
     # combine runs on a seeded expert-output tensor, so staging and combined
-    # rows are compared bit for bit with the oracle's
+    # rows are compared bit for bit with the oracle's; plan -> fused kernel ->
+    # combine run with and without programmatic dependent launches
     H, N = 128, 320
     with _handle(k_slices=2) as h:
         h.set_option(tovl.OPT_PRODUCER_MODE, mode)
+        h.set_option(tovl.OPT_PDL, pdl)
+        assert h.get_option(tovl.OPT_PDL) == pdl
         R = 0
         for r in range(1, 4):
             topk_np, E = ROUTINGS[routing](workloads.round_seed(2, r))
