@@ -58,6 +58,7 @@ def _load():
                 "oracle_dispatch": ([P, I, I, P, I, L, P], None),
                 "oracle_copy_perm": ([P, L, I, P, P], None),
                 "oracle_combine": ([P, I, P, P, I, I, P, P], None),
+                "oracle_reduce_partials": ([P, I, L, I, P], None),
                 "oracle_matmul_f32": ([P, P, I, I, I, P], None),
                 "oracle_matmul_rows_f32": ([P, P, I, I, P, I, P], None),
                 "oracle_grouped_matmul_f32": ([P, P, I, P, I, I, P], None),
@@ -146,6 +147,28 @@ def combine(Y, dst, w):
     C = np.empty((T, N), np.uint16)
     _load().oracle_combine(_p(Y), N, _p(dst), _p(w), T, k, _p(S), _p(C))
     return S, C
+
+
+def reduce_partials(P) -> np.ndarray:
+    """``O[m] = bf16(sum_s f32(P[s, m]))``, fp32 sums in ascending s; ``P`` is
+    [S, M, N] uint16 bf16 bits."""
+    P = _u16(P)
+    S, M, N = P.shape
+    O = np.empty((M, N), np.uint16)
+    _load().oracle_reduce_partials(_p(P), S, M, N, _p(O))
+    return O
+
+
+def gemm_reduce_scatter(X, W):
+    """Row-parallel layer on logical shards: ``P_s = bf16(X_s W_s)`` (fp32
+    accumulation, ascending k) and ``O = reduce_partials(P)``.  ``X`` is
+    [S, M, Ks], ``W`` [S, Ks, N], both uint16 bf16 bits.  Returns (P, O)."""
+    X = _u16(X)
+    W = _u16(W)
+    S, M, Ks = X.shape
+    assert W.shape[0] == S and W.shape[1] == Ks
+    P = np.stack([f32_to_bf16(matmul_f32(X[s], W[s])) for s in range(S)])
+    return P, reduce_partials(P)
 
 
 def copy_perm(src, perm) -> np.ndarray:

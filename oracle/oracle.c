@@ -20,6 +20,8 @@
  *   gather        G[s*R + i, :] = X_s[i, :]
  *   dispatch      D[dst(t,j), :] = x[t, :], every other row zero
  *   copy_perm     dst[perm[i], :] = src[i, :]
+ *   reduce        O[m, :] = bf16( sum_{s=0..S-1} f32(P_s[m, :]) ), fp32 sums in
+ *                 ascending s (the reduce-scatter that follows a K-split GEMM)
  *   combine       S[t*k + j, :] = Y[dst(t,j), :]  (token-ordered staging) and
  *                 C[t, :] = bf16( sum_{j=0..k-1} w[t,j] * f32(S[t*k + j, :]) ),
  *                 each product and each sum rounded to fp32 in ascending j
@@ -156,6 +158,25 @@ void oracle_combine(const uint16_t *Y, int N, const int32_t *dst, const float *w
                 acc = acc + prod;
             }
             C[(int64_t)t * N + n] = f32_to_bf16_rne(acc);
+        }
+}
+
+/* Reduction of S partial products, the reduce half of a row-parallel
+ * layer's reduce-scatter (ReduceScatter is the collective the platform page
+ * [P4 section 3] benchmarks beside AllGather).  Shard s holds the partial
+ * P_s = bf16(X_s W_s) of its K-slice; the output row m is the sum over
+ * shards.  Readings where the pages are silent: partials travel as bf16 (the
+ * rounded output of each shard's GEMM), the sum runs over s in ascending
+ * order with every partial sum rounded to fp32, and the result is rounded
+ * to bf16, nearest even.  P is [S][M][N], O is [M][N]. */
+void oracle_reduce_partials(const uint16_t *P, int S, int64_t M, int N, uint16_t *O)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int s = 0; s < S; ++s)
+                acc = acc + bf16_to_f32(P[((int64_t)s * M + m) * N + n]);
+            O[m * N + n] = f32_to_bf16_rne(acc);
         }
 }
 

@@ -366,3 +366,51 @@ def test_combine_within_fp32_bound_of_float64():
     got = _f64_from_bits(C)
     bound = 2 * k * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(exact) + 1e-30
     assert np.all(np.abs(got - exact) <= bound)
+
+
+# ------------------------------------------------------------------ reduce-scatter
+def test_reduce_partials_hand_worked():
+    P = _bf16_bits_from_f32(np.array([[[1, 2, -3]], [[0.5, 2, 3]], [[0.25, -8, 1]]], np.float32))
+    O = oracle.reduce_partials(P)
+    assert np.array_equal(O, _bf16_bits_from_f32(np.array([[1.75, -4, 1]], np.float32)))
+
+
+def test_reduce_partials_single_shard_is_identity():
+    P = np.random.default_rng(3).integers(0, 0x7F00, size=(1, 17, 9), dtype=np.uint16)
+    assert np.array_equal(oracle.reduce_partials(P), P[0])
+
+
+def test_reduce_partials_accumulate_in_fp32():
+    # 1 + 2^-8 + 2^-25 exactly lies just above the bf16 tie 1 + 2^-8 and rounds
+    # up to 1 + 2^-7; in fp32 the 2^-25 (a quarter unit in the last place) is
+    # lost in every order, the sum is the tie itself and rounds to even, 1.0
+    P = _bf16_bits_from_f32(np.array([[[1.0]], [[2.0 ** -8]], [[2.0 ** -25]]], np.float32))
+    assert _f64_from_bits(oracle.reduce_partials(P))[0, 0] == 1.0
+
+
+def test_gemm_reduce_scatter_is_the_k_split_gemm():
+    # small integers: every partial product is exact in bf16 and every sum in
+    # fp32, so the shard sum equals the one GEMM over the whole K exactly
+    rng = np.random.default_rng(4)
+    S, M, Ks, N = 3, 10, 8, 12
+    Xf = rng.integers(-2, 3, size=(S, M, Ks)).astype(np.float32)
+    Wf = rng.integers(-2, 3, size=(S, Ks, N)).astype(np.float32)
+    P, O = oracle.gemm_reduce_scatter(_bf16_bits_from_f32(Xf), _bf16_bits_from_f32(Wf))
+    full = np.concatenate(list(Xf), axis=1) @ np.concatenate(list(Wf), axis=0)
+    assert np.array_equal(_f64_from_bits(O), full)
+    for s in range(S):
+        assert np.array_equal(_f64_from_bits(P[s]), Xf[s] @ Wf[s])
+
+
+def test_gemm_reduce_scatter_within_bound_of_float64():
+    rng = np.random.default_rng(5)
+    S, M, Ks, N = 4, 16, 64, 24
+    X = _bf16_bits_from_f32(rng.standard_normal((S, M, Ks)).astype(np.float32))
+    W = _bf16_bits_from_f32((rng.standard_normal((S, Ks, N)) / 8).astype(np.float32))
+    _, O = oracle.gemm_reduce_scatter(X, W)
+    Xd, Wd = _f64_from_bits(X), _f64_from_bits(W)
+    exact = sum(Xd[s] @ Wd[s] for s in range(S))
+    mag = sum(np.abs(Xd[s]) @ np.abs(Wd[s]) for s in range(S))
+    # each partial: fp32 sum then bf16 rounding; then an fp32 sum of S terms and a final bf16 rounding
+    bound = (Ks * 2.0 ** -24 + 2.0 ** -8) * mag + S * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(exact) + 1e-30
+    assert np.all(np.abs(_f64_from_bits(O) - exact) <= bound)
