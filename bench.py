@@ -411,6 +411,38 @@ def combine_bench(h, cfg, y, timer, rounds: int, dev):
             "l2": "flushed before every call (expert outputs start in HBM)"}
 
 
+def rs_bench(cfg, rounds: int, dev, producers_sweep=(0, 16, 24, 32, 48)):
+    """GEMM + reduce-scatter on the TP shape split four ways along K: shard s
+    multiplies X_s [M][K/S] by W_s [K/S][N]; the S partials are reduced.
+    Algorithmic TFLOP/s = 2*M*N*K / time; reduction GB/s = (S+1)*M*N*2 / time."""
+    import torch
+    import workloads
+    from consumer_movement_gemm_gb300 import tovl
+    S, M, K, N = cfg.shards, cfg.M, cfg.K, cfg.N
+    Ks = K // S
+    X = workloads.bf16_normal((S, M, Ks), 1 / K ** 0.5, 0, dev)
+    W = workloads.bf16_normal((S, Ks, N), 1 / K ** 0.5, 1, dev)
+    partials = torch.empty(S, M, N, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    res = []
+    with tovl.Handle(0, max_rows=1 << 14, k_slices=4) as h:
+        timer = Timer(torch.cuda.current_stream())
+        for P in producers_sweep:
+            h.set_option(tovl.OPT_PRODUCERS, P)
+            fn = lambda: h.gemm_reduce_scatter(X, W, partials, out)  # noqa: E731
+            timer.time_calls(fn, 3)
+            ms = statistics.mean(timer.time_calls(fn, rounds))
+            assert h.sync_status() == 0
+            res.append({"producer_ctas": h.get_option(tovl.OPT_PRODUCERS), "consumer_ctas": h.get_option(tovl.OPT_CONSUMERS),
+                        "ms": ms, "TFLOP/s": cfg.flops / (ms * 1e-3) / 1e12,
+                        "reduce_GBps": (S + 1) * M * N * 2 / (ms * 1e-3) / 1e9, "auto": P == 0})
+    best = max(res, key=lambda r: r["TFLOP/s"])
+    return {"workload": f"GEMM + reduce-scatter: {S} shards, M={M}, K={K} (K/S={Ks} per shard), N={N}",
+            "TFLOP/s": res[0]["TFLOP/s"], "ms_per_round": res[0]["ms"], "producer_ctas": res[0]["producer_ctas"],
+            "best_sweep_TFLOP/s": best["TFLOP/s"], "sweep": res, "rounds": rounds,
+            "l2": "flushed before every round"}
+
+
 def copy_sweep(rounds: int, dev, sizes):
     import numpy as np
     import torch
@@ -512,6 +544,7 @@ def run_tovl(args):
                                                    dev, args.producers, args.k_slices)
         extra["dispatch_zipf"] = dispatch_bench(workloads.SKEWED, 20 if not args.full else workloads.SKEWED.rounds * 10,
                                                 dev, args.producers, args.k_slices)
+        extra["gemm_reduce_scatter"] = rs_bench(workloads.TP, 30 if not args.full else 200, dev)
         sizes = list(workloads.COPY.row_sizes)
         extra["gated_copy"] = copy_sweep(1000 if args.full else 20, dev, sizes)
 

@@ -35,9 +35,11 @@ __device__ __forceinline__ int gather_rows(const FusedParams& p)
     return (p.rows_valid && p.rows_valid[1] <= 0) ? 0 : p.M;
 }
 
+// Row blocks of a round (for reduce-scatter: of one shard).
 __device__ __forceinline__ int num_row_blocks(const FusedParams& p)
 {
     if (p.mode == kModeGather) return (gather_rows(p) + kTileM - 1) / kTileM;
+    if (p.mode == kModeReduceScatter) return p.M / kTileM;
     return p.meta[1];
 }
 

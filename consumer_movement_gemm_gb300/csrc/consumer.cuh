@@ -75,12 +75,29 @@ __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
 
 // Tiles of this consumer unit (a CTA, or a CTA pair): unit u of n_units
 // takes tiles u, u + n_units, ...; a tile covers PAIR consecutive row blocks
-// and one 256-column block.
+// and one 256-column block.  For a reduce-scatter round tile t is shard
+// t % S's partial of output tile t / S, so the S partials of one output tile
+// are computed side by side.
 template <int PAIR>
 struct Schedule {
     int unit, n_units, n_tiles;
     uint32_t rank;
-    __device__ int row_block(const FusedParams& p, int t) const { return (t / p.n_nb) * PAIR + static_cast<int>(rank); }
+    __device__ int out_tile(const FusedParams& p, int t) const
+    {
+        return p.mode == kModeReduceScatter ? t / p.n_shards : t;
+    }
+    __device__ int shard(const FusedParams& p, int t) const { return p.mode == kModeReduceScatter ? t % p.n_shards : 0; }
+    __device__ int row_block(const FusedParams& p, int t) const
+    {
+        return (out_tile(p, t) / p.n_nb) * PAIR + static_cast<int>(rank);
+    }
+    __device__ int col_block(const FusedParams& p, int t) const { return out_tile(p, t) % p.n_nb; }
+    // first row of this CTA's part of the tile in the A and output tensors
+    // (reduce-scatter: shard s's rows start at s * M)
+    __device__ int a_row(const FusedParams& p, int t) const
+    {
+        return shard(p, t) * (p.mode == kModeReduceScatter ? p.M : 0) + row_block(p, t) * kTileM;
+    }
 };
 
 template <int PAIR>
@@ -90,7 +107,7 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     sc.rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
     sc.unit = cid / PAIR;
     sc.n_units = p.n_consumers / PAIR;
-    sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb;
+    sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb * (p.mode == kModeReduceScatter ? p.n_shards : 1);
     return sc;
 }
 
@@ -156,8 +173,9 @@ __device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR
 {
     if (b.t >= sc.n_tiles) return;
     const int mb = sc.row_block(p, b.t);
-    b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K : 0;
-    b.n0 = (b.t % p.n_nb) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+    b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
+           : (p.mode == kModeReduceScatter) ? sc.shard(p, b.t) * p.K : 0;
+    b.n0 = sc.col_block(p, b.t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
 }
 
 // Arm the cursor's stage and issue its B boxes (the stage must be free).
@@ -249,7 +267,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     int a_count = 0;
     int gate_idx = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
-        const int mb = sc.row_block(p, t);
+        const int arow = sc.a_row(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
                 if (!wait_gate<PAIR>(p, s, sc, b, a_count, gate_idx)) return;
@@ -263,10 +281,10 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 if (!b_run<PAIR>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
                 if (PAIR == 1) {
-                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, mb * kTileM);
+                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow);
                 } else {
                     const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
-                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, mb * kTileM);
+                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, arow);
                 }
                 ++a_count;
                 if (++stage == T::kStages) stage = 0;
@@ -341,8 +359,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint32_t swz = (lane >> 1) & 3u;
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
-        const int mb = sc.row_block(p, t);
-        const int nb = t % p.n_nb;
+        const int arow = sc.a_row(p, t);
+        const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
@@ -387,9 +405,24 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             __syncwarp();
             if (lane == 0) {
                 ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                  mb * kTileM + q * 32);
+                                  arow + q * 32);
                 ptx::bulk_commit();
             }
+        }
+        if (p.mode == kModeReduceScatter) {
+            // Publish the partial tile ("cross-GPU sync protocols on PCIe",
+            // section 3): once this warp's stores have written global memory,
+            // it arrives on the tile's counter with its share of the
+            // 64-unit quota; the arrival that completes the count is elected
+            // and release-stores the sequence into the tile's slot.
+            if (lane == 0) {
+                ptx::bulk_wait<0>();
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
+            static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
+            if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
+            __syncwarp();
         }
         if (p.stats && lane == 0) {
             const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;

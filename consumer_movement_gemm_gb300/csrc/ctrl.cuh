@@ -102,7 +102,7 @@ struct Plan {
     int* meta;            // [4] m_pad, n_blocks, zero_padding, error
 };
 
-enum : int { kModeGather = 0, kModeDispatch = 1 };
+enum : int { kModeGather = 0, kModeDispatch = 1, kModeReduceScatter = 2 };
 
 struct FusedParams {
     CUtensorMap tmap_a;   // A: gathered / dispatched rows [rows][K] bf16, box 64 x 128, 128B swizzle
@@ -144,6 +144,11 @@ struct FusedParams {
     void* combined;       // [T][N] bf16 combined rows
     int n_reducers;
     int T, k;
+    // reduce-scatter: consumers write shard partials (out, [S][M][N]) and
+    // publish each partial tile; producers sum the S partials into rs_out
+    int rs_tiles;         // partial tiles: S x output tiles; tile t publishes counter t
+    int rs_pair;          // rows of an output tile / 128
+    void* rs_out;         // [M][N] bf16
     // destinations
     void* gathered;       // gathered / dispatched buffer
     void* out;            // [rows][N] bf16

@@ -83,11 +83,13 @@ __device__ inline void seed_counters(const FusedParams& p, int gw, int n_gw, boo
         const int ch = cs / S, sl = cs - ch * S;
         int real = 0;
         if (p.mode == kModeGather && sl < p.k_slices) real = min(max(gather_rows(p) - ch * kChunkRows, 0), kChunkRows);
+        // reduce-scatter: counter t collects the quota from partial tile t's epilogue warps
+        if (p.mode == kModeReduceScatter && cs < p.rs_tiles) real = kChunkRows;
         const bool is_completion = real > 0 && real < kChunkRows;
         if (is_completion == completion && real < kChunkRows) arrive_and_publish(c, cs, kChunkRows - real, p.seq);
     }
     // block-slice counters
-    if (p.mode == kModeGather) {
+    if (p.mode == kModeGather || p.mode == kModeReduceScatter) {
         if (!completion)
             for (int bs = gw * 32 + lane; bs < c.n_block_cap * S; bs += n_gw * 32)
                 ptx::red_add_release_gpu(c.rbcnt + bs, kBlockRows);
@@ -309,6 +311,64 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
     }
 }
 
+// Reduce-scatter producers: item = 8 rows x 256 columns of one output tile,
+// in the consumers' tile order.  A warp waits until the S partial tiles of
+// its output tile are published (lane s polls tile s's slot with acquire
+// loads; warp vote), then sums the S bf16 partials of its rows in fp32,
+// ascending s, and stores the bf16 result.  Lane l owns the 16-byte column
+// group l of each row (32 groups = 256 columns).
+__device__ inline void rs_reduce(const FusedParams& p, int gw, int n_gw)
+{
+    constexpr int kRows = 8;
+    const int lane = static_cast<int>(ptx::lane_id());
+    const int S = p.n_shards;
+    const int M = p.M;
+    const int tile_rows = kTileM * p.rs_pair;
+    const int per_tile = tile_rows / kRows;
+    const int n_out = p.rs_tiles / S;
+    const size_t row_bytes = static_cast<size_t>(p.N) * 2;
+    const uint8_t* part = static_cast<const uint8_t*>(p.out);
+    uint8_t* out = static_cast<uint8_t*>(p.rs_out);
+    for (int i = gw; i < n_out * per_tile; i += n_gw) {
+        const int u = i / per_tile;
+        const int r0 = (u / p.n_nb) * tile_rows + (i - u * per_tile) * kRows;
+        if (r0 >= M) continue;
+        const int* mine = lane < S ? p.ctrl.slot + u * S + lane : nullptr;
+        if (warp_wait_lanes(mine, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
+        const size_t col = static_cast<size_t>(u % p.n_nb) * kTileN * 2 + static_cast<size_t>(lane) * 16;
+        float acc[kRows][8];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[j][c] = 0.0f;
+        for (int s = 0; s < S; ++s) {
+            int4 v[kRows];
+#pragma unroll
+            for (int j = 0; j < kRows; ++j)
+                v[j] = ptx::ld_v4(reinterpret_cast<const int4*>(part + (static_cast<size_t>(s) * M + r0 + j) * row_bytes + col));
+#pragma unroll
+            for (int j = 0; j < kRows; ++j) {
+                const uint32_t w[4] = {static_cast<uint32_t>(v[j].x), static_cast<uint32_t>(v[j].y),
+                                       static_cast<uint32_t>(v[j].z), static_cast<uint32_t>(v[j].w)};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc[j][2 * c] = __fadd_rn(acc[j][2 * c], __uint_as_float(w[c] << 16));
+                    acc[j][2 * c + 1] = __fadd_rn(acc[j][2 * c + 1], __uint_as_float(w[c] & 0xffff0000u));
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            int4 o;
+            o.x = static_cast<int>(ptx::pack_bf16x2(acc[j][0], acc[j][1]));
+            o.y = static_cast<int>(ptx::pack_bf16x2(acc[j][2], acc[j][3]));
+            o.z = static_cast<int>(ptx::pack_bf16x2(acc[j][4], acc[j][5]));
+            o.w = static_cast<int>(ptx::pack_bf16x2(acc[j][6], acc[j][7]));
+            ptx::st_v4(reinterpret_cast<int4*>(out + static_cast<size_t>(r0 + j) * row_bytes + col), o);
+        }
+    }
+}
+
 __device__ inline void producer(const FusedParams& p, uint8_t* smem, int pid)
 {
     const int warp = threadIdx.x / 32;
@@ -321,7 +381,9 @@ __device__ inline void producer(const FusedParams& p, uint8_t* smem, int pid)
     // sources, plan and counters were written by earlier kernels
     ptx::grid_dep_wait();
     seed_counters(p, gw, n_gw, true);
-    if (p.producer_mode == 1) {
+    if (p.mode == kModeReduceScatter) {
+        rs_reduce(p, gw, n_gw);
+    } else if (p.producer_mode == 1) {
         if (p.item_rows <= 16) copy_items_staged<1>(p, smem, gw, n_gw);
         else if (p.item_rows == 32) copy_items_staged<2>(p, smem, gw, n_gw);
         else copy_items_staged<4>(p, smem, gw, n_gw);

@@ -55,11 +55,21 @@ __device__ __forceinline__ bool arrive_and_publish(const Ctrl& ctrl, int c, int 
 // next (bar.warp.sync orders memory among its threads), so lane 0 may hand
 // the gate on without reading the words again.  Returns the number of
 // polling rounds, negative on timeout or abort.
+__device__ __forceinline__ int warp_wait_lanes(const int* mine, int target, const Ctrl& ctrl, int seq,
+                                               long long timeout_ns);
+
 __device__ __forceinline__ int warp_wait_ge(const int* const* words, int n, int target, const Ctrl& ctrl, int seq,
                                             long long timeout_ns)
 {
     const uint32_t lane = ptx::lane_id();
-    const int* mine = (static_cast<int>(lane) < n) ? words[lane] : nullptr;
+    return warp_wait_lanes((static_cast<int>(lane) < n) ? words[lane] : nullptr, target, ctrl, seq, timeout_ns);
+}
+
+// The same wait with each lane naming its own word (nullptr: none).
+__device__ __forceinline__ int warp_wait_lanes(const int* mine, int target, const Ctrl& ctrl, int seq,
+                                               long long timeout_ns)
+{
+    const uint32_t lane = ptx::lane_id();
     uint64_t start = 0;
     int rounds = 0;
     uint32_t backoff = 32;

@@ -617,6 +617,70 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     return TOVL_OK;
 }
 
+TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shards, int M, int Ks, const void* W,
+                                      int N, void* partials, void* out, void* stream)
+{
+    if (!h) return TOVL_ERR_INVALID;
+    if (!X || !W || !partials || !out) return TOVL_ERR_INVALID;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(partials) || !aligned16(out)) return TOVL_ERR_INVALID;
+    if (num_shards < 1 || num_shards > kMaxShards || M < 1 || Ks < kTileK || Ks % kTileK) return TOVL_ERR_INVALID;
+    if (M % kTileM || Ks > kMaxK || N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
+    // CTA pairs need whole 256-row tiles inside every shard
+    const int pair = (h->pair_mode && h->max_pairs > 0 && (M / kTileM) % 2 == 0) ? 2 : 1;
+    const int n_mb = M / kTileM;
+    const int n_nb = N / kTileN;
+    const long long out_tiles = static_cast<long long>(n_mb / pair) * n_nb;
+    const long long tiles = out_tiles * num_shards;
+    if (tiles > static_cast<long long>(h->ctrl.n_chunk_cap) * h->ctrl.n_slices) return TOVL_ERR_INVALID;
+    DeviceGuard g(h->device);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FusedParams p;
+    base_params(h, p);
+    p.mode = kModeReduceScatter;
+    p.M = M;
+    p.N = N;
+    p.K = Ks;
+    p.n_kb = Ks / kTileK;
+    p.n_nb = n_nb;
+    p.row_bytes = N * 2;
+    p.n_shards = num_shards;
+    p.rows_per_shard = M;
+    p.rs_tiles = static_cast<int>(tiles);
+    p.rs_pair = pair;
+    p.rs_out = out;
+    p.out = partials;
+    p.out_rows = num_shards * M;
+    // reduction traffic: S partial rows read and one output row written per row
+    int P, C;
+    split_ctas(h, P, C, n_mb, n_nb * num_shards, 2.0 * (num_shards + 1) * M * N,
+               2.0 * num_shards * static_cast<double>(M) * N * Ks, pair);
+    p.n_producers = P;
+    p.n_consumers = C;
+    p.gated = 0;
+    p.k_slices = 1;
+    p.item_rows = 1;
+    p.wave_blocks = 1;
+    int rc;
+    if ((rc = encode_2d(h, &p.tmap_a, X, Ks, static_cast<uint64_t>(num_shards) * M, static_cast<uint64_t>(Ks) * 2,
+                        kTileK, kTileM)) != TOVL_OK)
+        return rc;
+    if ((rc = encode_2d(h, &p.tmap_b, W, N, static_cast<uint64_t>(num_shards) * Ks, static_cast<uint64_t>(N) * 2, 64,
+                        kTileK)) != TOVL_OK)
+        return rc;
+    if ((rc = encode_2d(h, &p.tmap_out, partials, N, static_cast<uint64_t>(num_shards) * M,
+                        static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
+        return rc;
+    p.seq = static_cast<int>(h->seq + 1);
+    p.gate_seq = p.seq + h->fault_gate_offset;
+    p.trace_tiles = static_cast<int>(tiles);
+    if ((rc = reset_stats(h, s, tiles, 1)) != TOVL_OK) return rc;
+    const cudaError_t e = launch(h, p, s, true, pair);
+    if (e != cudaSuccess) return cuda_fail(h, e, "reduce-scatter launch");
+    h->seq += 1;
+    h->last_stream = s;
+    return TOVL_OK;
+}
+
 TOVL_API int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void* staging, void* combined,
                           void* stream)
 {

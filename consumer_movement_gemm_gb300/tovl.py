@@ -81,6 +81,7 @@ SIGNATURES = {
     "tovl_dispatch_rows": ([_I, _I, _I], _LL),
     "tovl_dispatch_grouped_gemm": ([_P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _P, _P], _I),
     "tovl_combine": ([_P, _P, _I, _P, _P, _P, _P], _I),
+    "tovl_gemm_reduce_scatter": ([_P, _P, _I, _I, _I, _P, _I, _P, _P, _P], _I),
     "tovl_gemm_only": ([_P, _P, _I, _I, _P, _I, _P, _P], _I),
     "tovl_copy_only": ([_P, ctypes.POINTER(_P), _I, _I, _I, _P, _P], _I),
     "tovl_gated_copy": ([_P, _P, _P, _LL, _I, _P, _I, _I, _P], _I),
@@ -222,6 +223,15 @@ class Handle:
         ptrs, S, R, K = _shard_ptrs(shards)
         rc = load().tovl_copy_only(self.h, ptrs, S, R, K, _ptr(gathered), _stream(stream))
         _check(self.h, rc, "tovl_copy_only")
+
+    def gemm_reduce_scatter(self, X, W, partials, out, stream=None):
+        """Row-parallel layer on logical shards: ``partials[s] = X[s] @ W[s]``
+        and ``out = sum_s partials[s]``.  X [S, M, Ks], W [S, Ks, N]."""
+        S, M, Ks = X.shape
+        N = W.shape[2]
+        rc = load().tovl_gemm_reduce_scatter(self.h, _ptr(X), S, M, Ks, _ptr(W), N, _ptr(partials), _ptr(out),
+                                             _stream(stream))
+        _check(self.h, rc, "tovl_gemm_reduce_scatter")
 
     def combine(self, y, gate_w, staging, combined, stream=None):
         """Combine of the last dispatch round: ``staging[t*k+j] = y[dst(t,j)]``

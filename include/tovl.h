@@ -135,6 +135,30 @@ int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const
                                const void* W, int N, void* dispatched, int* expert_offsets, void* out,
                                void* stream);
 
+/* GEMM + reduce-scatter over logical shards (a row-parallel layer: ReduceScatter
+ * is the collective the platform page benchmarks beside AllGather, section
+ * 3).  Shard s holds the K-slice X_s [M][Ks] of the activations and W_s
+ * [Ks][N] of the weights; its partial P_s = X_s x W_s is computed by the
+ * consumer CTAs (fp32 accumulation, rounded to bf16) and every partial tile
+ * is published with the single-writer protocol: its epilogue warps arrive on
+ * the tile's counter (acq_rel) once their stores are in global memory, and
+ * the last arrival release-stores the sequence into the tile's slot.  The
+ * producer CTAs poll the S slots of an output tile (acquire) and write
+ *   out[m][n] = bf16( sum_s f32(P_s[m][n]) ), fp32 sums in ascending s.
+ *   X           device, bf16 [S][M][Ks]
+ *   num_shards  S, 1..64
+ *   M           rows, a multiple of 128
+ *   Ks          multiple of 64, at most 32768
+ *   W           device, bf16 [S][Ks][N], N a multiple of 256
+ *   partials    device, bf16 [S][M][N]: receives P_s
+ *   out         device, bf16 [M][N]: receives the reduced rows (shard r owns
+ *               rows [r*M/S, (r+1)*M/S) when S divides M)
+ * Partial tiles (S x (M/128) x (N/256), or half that with CTA pairs) must
+ * not exceed max_rows/64 x k_slices, the handle's counter capacity.  One
+ * round (one sequence number). */
+int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shards, int M, int Ks, const void* W, int N,
+                             void* partials, void* out, void* stream);
+
 /* Combine: the reverse of the last dispatch round on this handle ("cross-GPU
  * sync protocols on PCIe", section 3, the layer-1 combine: every expert
  * output row goes back to its token's staging row; each 64-row staging chunk

@@ -338,6 +338,58 @@ def test_combine_timeout_and_rejected_plan():
         _check_ctrl(h, 5)
 
 
+# ------------------------------------------------------------------ GEMM + reduce-scatter
+def _rs_round(h, S, M, Ks, N, seed):
+    X = workloads.bf16_normal((S, M, Ks), 1 / math.sqrt(S * Ks), seed, DEV)
+    W = workloads.bf16_normal((S, Ks, N), 1.0, seed + 1, DEV)
+    partials = torch.full((S, M, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    out = torch.full((M, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    h.gemm_reduce_scatter(X, W, partials, out)
+    return X, W, partials, out
+
+
+@pytest.mark.parametrize("S,M,Ks,N,P", [(4, 512, 256, 512, 0), (1, 256, 128, 256, 0), (3, 384, 192, 768, 4),
+                                        (5, 128, 64, 256, 8), (2, 1024, 512, 1024, 16)])
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gemm_reduce_scatter(S, M, Ks, N, P, pairs):
+    # (3, 384): an odd number of row blocks runs single-CTA tiles even with pairs on
+    with _handle(producer_ctas=P, k_slices=4) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
+        for r in range(1, 3):
+            X, W, partials, out = _rs_round(h, S, M, Ks, N, 700 + r)
+            assert h.sync_status() == 0
+            Po, Oo = oracle.gemm_reduce_scatter(bits(X), bits(W))
+            for s in range(S):
+                assert_close(partials[s], oracle.bf16_to_f32(Po[s]), f"partial {s}")
+            assert_close(out, oracle.bf16_to_f32(Oo), "reduced")
+            _check_ctrl(h, r)
+
+
+def test_gemm_reduce_scatter_timeout_recovers():
+    with _handle(wait_timeout_ns=5_000_000, k_slices=2) as h:
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # reducers wait for a sequence nobody publishes
+        _rs_round(h, 2, 256, 128, 256, 1)
+        assert h.sync_status() == tovl.TOVL_ERR_TIMEOUT
+        h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 0)
+        X, W, partials, out = _rs_round(h, 2, 256, 128, 256, 2)
+        assert h.sync_status() == 0
+        _, Oo = oracle.gemm_reduce_scatter(bits(X), bits(W))
+        assert_close(out, oracle.bf16_to_f32(Oo), "after timeout")
+        _check_ctrl(h, 2)
+
+
+def test_gemm_reduce_scatter_rejects_shapes():
+    with _handle() as h:
+        X = torch.zeros(2, 100, 64, dtype=torch.bfloat16, device=DEV)
+        W = torch.zeros(2, 64, 256, dtype=torch.bfloat16, device=DEV)
+        P = torch.zeros(2, 100, 256, dtype=torch.bfloat16, device=DEV)
+        O = torch.zeros(100, 256, dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(tovl.TovlError):
+            h.gemm_reduce_scatter(X, W, P, O)                # M not a multiple of 128
+        assert h.sync_status() == 0
+        _check_ctrl(h, 0)
+
+
 # ------------------------------------------------------------------ gated copy
 @pytest.mark.parametrize("row_bytes", [256, 1024, 8192])
 @pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK])
