@@ -411,7 +411,7 @@ def combine_bench(h, cfg, y, timer, rounds: int, dev):
             "l2": "flushed before every call (expert outputs start in HBM)"}
 
 
-def rs_bench(cfg, rounds: int, dev, producers_sweep=(0, 16, 24, 32, 48)):
+def rs_bench(cfg, rounds: int, dev, producers_sweep=(0, 8, 16, 24, 32, 48), role_switch: int = 1):
     """GEMM + reduce-scatter on the TP shape split four ways along K: shard s
     multiplies X_s [M][K/S] by W_s [K/S][N]; the S partials are reduced.
     Algorithmic TFLOP/s = 2*M*N*K / time; reduction GB/s = (S+1)*M*N*2 / time."""
@@ -429,13 +429,15 @@ def rs_bench(cfg, rounds: int, dev, producers_sweep=(0, 16, 24, 32, 48)):
         timer = Timer(torch.cuda.current_stream())
         for P in producers_sweep:
             h.set_option(tovl.OPT_PRODUCERS, P)
+            h.set_option(tovl.OPT_ROLE_SWITCH, role_switch)
             fn = lambda: h.gemm_reduce_scatter(X, W, partials, out)  # noqa: E731
             timer.time_calls(fn, 3)
             ms = statistics.mean(timer.time_calls(fn, rounds))
             assert h.sync_status() == 0
             res.append({"producer_ctas": h.get_option(tovl.OPT_PRODUCERS), "consumer_ctas": h.get_option(tovl.OPT_CONSUMERS),
                         "ms": ms, "TFLOP/s": cfg.flops / (ms * 1e-3) / 1e12,
-                        "reduce_GBps": (S + 1) * M * N * 2 / (ms * 1e-3) / 1e9, "auto": P == 0})
+                        "reduce_GBps": (S + 1) * M * N * 2 / (ms * 1e-3) / 1e9, "auto": P == 0,
+                        "role_switch": role_switch})
     best = max(res, key=lambda r: r["TFLOP/s"])
     return {"workload": f"GEMM + reduce-scatter: {S} shards, M={M}, K={K} (K/S={Ks} per shard), N={N}",
             "TFLOP/s": res[0]["TFLOP/s"], "ms_per_round": res[0]["ms"], "producer_ctas": res[0]["producer_ctas"],

@@ -25,6 +25,7 @@
 #include "ctrl.cuh"
 #include "ptx.cuh"
 #include "sync.cuh"
+#include "producer.cuh"
 
 namespace tovl {
 
@@ -495,6 +496,9 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
     if (threadIdx.x == 0) stat_max(p, kStatConsEndNs, ptx::globaltimer());
+    // role switch: with its tiles done, every warp of the CTA takes
+    // reduction items from the round's ticket counter
+    if (p.mode == kModeReduceScatter && p.rs_join) rs_reduce(p);
 }
 
 }  // namespace tovl

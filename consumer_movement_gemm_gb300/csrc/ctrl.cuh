@@ -78,6 +78,7 @@ struct Ctrl {
     int* rbcnt;           // [n_block_cap]  row-block arrival counters
     int* status;          // [1] sticky error code
     int* abort_seq;       // [1] highest sequence that gave up waiting
+    int* work;            // [1] item tickets of a round whose items are shared out dynamically (zeroed per round)
     unsigned long long* stats;   // [kNumStats]
     long long* pub_ns;    // [n_chunk_cap * n_slices]  publish time of each chunk slice (stats / stamps)
     long long* obs_ns;    // [n_chunk_cap]  first observation time by a waiter (copy sweep)
@@ -148,6 +149,7 @@ struct FusedParams {
     // publish each partial tile; producers sum the S partials into rs_out
     int rs_tiles;         // partial tiles: S x output tiles; tile t publishes counter t
     int rs_pair;          // rows of an output tile / 128
+    int rs_join;          // consumers take reduction items once their tiles are done (role switch)
     void* rs_out;         // [M][N] bf16
     // destinations
     void* gathered;       // gathered / dispatched buffer

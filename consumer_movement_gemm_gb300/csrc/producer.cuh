@@ -311,60 +311,86 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
     }
 }
 
-// Reduce-scatter producers: item = 8 rows x 256 columns of one output tile,
-// in the consumers' tile order.  A warp waits until the S partial tiles of
-// its output tile are published (lane s polls tile s's slot with acquire
-// loads; warp vote), then sums the S bf16 partials of its rows in fp32,
-// ascending s, and stores the bf16 result.  Lane l owns the 16-byte column
-// group l of each row (32 groups = 256 columns).
-__device__ inline void rs_reduce(const FusedParams& p, int gw, int n_gw)
+// Reduce-scatter reduction.  An item is 16 rows x 256 columns of one output
+// tile; items are numbered in the consumers' tile order and handed out by a
+// per-round ticket counter, so any warp that is free -- a producer warp from
+// the start, a consumer warp once its CTA's tiles are done (the role switch)
+// -- takes the next one.  For each item the warp waits until the S partial
+// tiles of its output tile are published (lane s polls tile s's slot with
+// acquire loads; warp vote), then sums the S bf16 partials of its rows in
+// fp32, ascending s, and stores the bf16 result, four rows at a time.  Lane l
+// owns the 16-byte column group l of each row (32 groups = 256 columns).
+// Shards are read four at a time, so each lane has 16 loads in flight.
+__device__ inline void rs_reduce(const FusedParams& p)
 {
-    constexpr int kRows = 8;
+    constexpr int kItemRows = 16;
+    constexpr int kRows = 4;
+    constexpr int kShardsAtOnce = 4;
     const int lane = static_cast<int>(ptx::lane_id());
     const int S = p.n_shards;
     const int M = p.M;
     const int tile_rows = kTileM * p.rs_pair;
-    const int per_tile = tile_rows / kRows;
+    const int per_tile = tile_rows / kItemRows;
     const int n_out = p.rs_tiles / S;
+    const int n_items = n_out * per_tile;
     const size_t row_bytes = static_cast<size_t>(p.N) * 2;
+    const size_t shard_bytes = static_cast<size_t>(M) * row_bytes;
     const uint8_t* part = static_cast<const uint8_t*>(p.out);
     uint8_t* out = static_cast<uint8_t*>(p.rs_out);
-    for (int i = gw; i < n_out * per_tile; i += n_gw) {
+    for (;;) {
+        int i = 0;
+        if (lane == 0) i = ptx::atom_add_relaxed_gpu(p.ctrl.work, 1);
+        i = __shfl_sync(0xffffffffu, i, 0);
+        if (i >= n_items) break;
         const int u = i / per_tile;
-        const int r0 = (u / p.n_nb) * tile_rows + (i - u * per_tile) * kRows;
-        if (r0 >= M) continue;
+        const int item_r0 = (u / p.n_nb) * tile_rows + (i - u * per_tile) * kItemRows;
+        if (item_r0 >= M) continue;
         const int* mine = lane < S ? p.ctrl.slot + u * S + lane : nullptr;
         if (warp_wait_lanes(mine, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
         const size_t col = static_cast<size_t>(u % p.n_nb) * kTileN * 2 + static_cast<size_t>(lane) * 16;
-        float acc[kRows][8];
-#pragma unroll
-        for (int j = 0; j < kRows; ++j)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[j][c] = 0.0f;
-        for (int s = 0; s < S; ++s) {
-            int4 v[kRows];
+#pragma unroll 1
+        for (int r0 = item_r0; r0 < item_r0 + kItemRows; r0 += kRows) {
+            const uint8_t* base = part + static_cast<size_t>(r0) * row_bytes + col;
+            float acc[kRows][8];
 #pragma unroll
             for (int j = 0; j < kRows; ++j)
-                v[j] = ptx::ld_v4(reinterpret_cast<const int4*>(part + (static_cast<size_t>(s) * M + r0 + j) * row_bytes + col));
 #pragma unroll
-            for (int j = 0; j < kRows; ++j) {
-                const uint32_t w[4] = {static_cast<uint32_t>(v[j].x), static_cast<uint32_t>(v[j].y),
-                                       static_cast<uint32_t>(v[j].z), static_cast<uint32_t>(v[j].w)};
+                for (int c = 0; c < 8; ++c) acc[j][c] = 0.0f;
+            for (int s0 = 0; s0 < S; s0 += kShardsAtOnce) {
+                int4 v[kShardsAtOnce][kRows];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    acc[j][2 * c] = __fadd_rn(acc[j][2 * c], __uint_as_float(w[c] << 16));
-                    acc[j][2 * c + 1] = __fadd_rn(acc[j][2 * c + 1], __uint_as_float(w[c] & 0xffff0000u));
+                for (int q = 0; q < kShardsAtOnce; ++q) {
+                    // shards past S re-read the last one (unconditional loads; their sums are skipped)
+                    const int s = min(s0 + q, S - 1);
+#pragma unroll
+                    for (int j = 0; j < kRows; ++j)
+                        v[q][j] = ptx::ld_v4(reinterpret_cast<const int4*>(base + s * shard_bytes + j * row_bytes));
+                }
+#pragma unroll
+                for (int q = 0; q < kShardsAtOnce; ++q) {
+                    if (s0 + q >= S) break;
+#pragma unroll
+                    for (int j = 0; j < kRows; ++j) {
+                        const uint32_t w[4] = {static_cast<uint32_t>(v[q][j].x), static_cast<uint32_t>(v[q][j].y),
+                                               static_cast<uint32_t>(v[q][j].z), static_cast<uint32_t>(v[q][j].w)};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            acc[j][2 * c] = __fadd_rn(acc[j][2 * c], __uint_as_float(w[c] << 16));
+                            acc[j][2 * c + 1] = __fadd_rn(acc[j][2 * c + 1], __uint_as_float(w[c] & 0xffff0000u));
+                        }
+                    }
                 }
             }
-        }
+            uint8_t* dst = out + static_cast<size_t>(r0) * row_bytes + col;
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-            int4 o;
-            o.x = static_cast<int>(ptx::pack_bf16x2(acc[j][0], acc[j][1]));
-            o.y = static_cast<int>(ptx::pack_bf16x2(acc[j][2], acc[j][3]));
-            o.z = static_cast<int>(ptx::pack_bf16x2(acc[j][4], acc[j][5]));
-            o.w = static_cast<int>(ptx::pack_bf16x2(acc[j][6], acc[j][7]));
-            ptx::st_v4(reinterpret_cast<int4*>(out + static_cast<size_t>(r0 + j) * row_bytes + col), o);
+            for (int j = 0; j < kRows; ++j) {
+                int4 o;
+                o.x = static_cast<int>(ptx::pack_bf16x2(acc[j][0], acc[j][1]));
+                o.y = static_cast<int>(ptx::pack_bf16x2(acc[j][2], acc[j][3]));
+                o.z = static_cast<int>(ptx::pack_bf16x2(acc[j][4], acc[j][5]));
+                o.w = static_cast<int>(ptx::pack_bf16x2(acc[j][6], acc[j][7]));
+                ptx::st_v4(reinterpret_cast<int4*>(dst + j * row_bytes), o);
+            }
         }
     }
 }
@@ -382,7 +408,7 @@ __device__ inline void producer(const FusedParams& p, uint8_t* smem, int pid)
     ptx::grid_dep_wait();
     seed_counters(p, gw, n_gw, true);
     if (p.mode == kModeReduceScatter) {
-        rs_reduce(p, gw, n_gw);
+        rs_reduce(p);
     } else if (p.producer_mode == 1) {
         if (p.item_rows <= 16) copy_items_staged<1>(p, smem, gw, n_gw);
         else if (p.item_rows == 32) copy_items_staged<2>(p, smem, gw, n_gw);

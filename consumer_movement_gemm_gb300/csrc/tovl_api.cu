@@ -43,6 +43,7 @@ struct tovl_ctx {
     bool coop_enabled = true;  // fused launches ask for the co-residency guarantee
     int producer_mode = 0;     // fused producers: 0 vector copies, 1 staged bulk loads
     bool pdl = true;           // programmatic dependent launch between this library's kernels
+    bool role_switch = true;   // reduce-scatter consumers join the reduction after their tiles
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
     Ctrl ctrl{};
@@ -145,6 +146,7 @@ static void carve_ctrl(Carve& c, Ctrl& ctrl, int n_chunks, int n_blocks, int S)
     ctrl.rbcnt = c.take<int>(static_cast<size_t>(n_blocks) * S);
     ctrl.status = c.take<int>(1);
     ctrl.abort_seq = c.take<int>(1);
+    ctrl.work = c.take<int>(1);
     ctrl.stats = c.take<unsigned long long>(kNumStats);
     ctrl.pub_ns = c.take<long long>(static_cast<size_t>(n_chunks) * S);
     ctrl.obs_ns = c.take<long long>(n_chunks);
@@ -647,6 +649,7 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     p.rows_per_shard = M;
     p.rs_tiles = static_cast<int>(tiles);
     p.rs_pair = pair;
+    p.rs_join = h->role_switch ? 1 : 0;
     p.rs_out = out;
     p.out = partials;
     p.out_rows = num_shards * M;
@@ -654,6 +657,20 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     int P, C;
     split_ctas(h, P, C, n_mb, n_nb * num_shards, 2.0 * (num_shards + 1) * M * N,
                2.0 * num_shards * static_cast<double>(M) * N * Ks, pair);
+    if (h->producers == 0 && h->role_switch) {
+        // the consumers take over the reduction once their tiles are done, so
+        // the producers only need to keep pace while the GEMM runs: about a
+        // tenth of the SMs (measured on the TP shape: 16 of 152 best)
+        P = (h->num_sms / 10 + 1) & ~1;
+        if (P < 2) P = 2;
+        C = h->num_sms - P;
+        if (pair == 2) {
+            if (C > 2 * h->max_pairs) C = 2 * h->max_pairs;
+            C &= ~1;
+        }
+        h->last_P = P;
+        h->last_C = C;
+    }
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 0;
@@ -674,7 +691,10 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     p.gate_seq = p.seq + h->fault_gate_offset;
     p.trace_tiles = static_cast<int>(tiles);
     if ((rc = reset_stats(h, s, tiles, 1)) != TOVL_OK) return rc;
-    const cudaError_t e = launch(h, p, s, true, pair);
+    // the reduction items are handed out by a ticket counter that starts at 0
+    cudaError_t e = cudaMemsetAsync(h->ctrl.work, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "ticket reset");
+    e = launch(h, p, s, true, pair);
     if (e != cudaSuccess) return cuda_fail(h, e, "reduce-scatter launch");
     h->seq += 1;
     h->last_stream = s;
@@ -959,6 +979,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != 0 && value != 1) return TOVL_ERR_INVALID;
         h->pdl = value != 0;
         return TOVL_OK;
+    case 16:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->role_switch = value != 0;
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -983,6 +1007,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 13: *value = h->coop_enabled ? 1 : 0; return TOVL_OK;
     case 14: *value = h->producer_mode; return TOVL_OK;
     case 15: *value = (h->pdl && h->pdl_ok) ? 1 : 0; return TOVL_OK;
+    case 16: *value = h->role_switch ? 1 : 0; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

@@ -39,6 +39,7 @@ OPT_COOP_PAIRS = 12
 OPT_COOPERATIVE = 13
 OPT_PRODUCER_MODE = 14
 OPT_PDL = 15
+OPT_ROLE_SWITCH = 16
 
 
 class TovlError(RuntimeError):

@@ -365,6 +365,18 @@ def test_gemm_reduce_scatter(S, M, Ks, N, P, pairs):
             _check_ctrl(h, r)
 
 
+@pytest.mark.parametrize("S,M,Ks,N,P", [(4, 512, 256, 512, 0), (3, 384, 192, 768, 4)])
+def test_gemm_reduce_scatter_without_role_switch(S, M, Ks, N, P):
+    with _handle(producer_ctas=P, k_slices=4) as h:
+        h.set_option(tovl.OPT_ROLE_SWITCH, 0)
+        for r in range(1, 3):
+            X, W, partials, out = _rs_round(h, S, M, Ks, N, 800 + r)
+            assert h.sync_status() == 0
+            _, Oo = oracle.gemm_reduce_scatter(bits(X), bits(W))
+            assert_close(out, oracle.bf16_to_f32(Oo), "reduced")
+            _check_ctrl(h, r)
+
+
 def test_gemm_reduce_scatter_timeout_recovers():
     with _handle(wait_timeout_ns=5_000_000, k_slices=2) as h:
         h.set_option(tovl.OPT_FAULT_GATE_OFFSET, 1)      # reducers wait for a sequence nobody publishes
