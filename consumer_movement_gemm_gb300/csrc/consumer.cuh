@@ -54,7 +54,13 @@ struct ConsumerSmem {
     uint64_t* tempty;    // epilogue -> MMA (in the pair's first CTA: both CTAs' warps)
     uint32_t* tmem_slot;
     int* gates_passed;   // gate warp -> TMA warp: number of (tile, slice) gates passed
+    int* ring;           // dynamic schedule: kRing tile indices handed to the other roles (-1 = no more)
+    int* ring_head;      // entries published
+    int* epi_started;    // epilogue warps' tile starts (kEpiWarps per tile): ring entries that are free
+    int* tma_done;       // tiles whose loads the TMA warp has all issued
 };
+
+constexpr int kRing = 8;
 
 template <int PAIR>
 __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
@@ -71,6 +77,10 @@ __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
     s.tempty = bars + 2 * T::kStages + 2;
     s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * T::kStages + 4);
     s.gates_passed = reinterpret_cast<int*>(bars + 2 * T::kStages + 5);
+    s.ring = reinterpret_cast<int*>(bars + 2 * T::kStages + 6);
+    s.ring_head = s.ring + kRing;
+    s.epi_started = s.ring_head + 1;
+    s.tma_done = s.ring_head + 2;
     return s;
 }
 
@@ -83,6 +93,7 @@ template <int PAIR>
 struct Schedule {
     int unit, n_units, n_tiles;
     uint32_t rank;
+    bool dyn;            // tiles come from the ticket counter through the ring (single CTAs only)
     __device__ int out_tile(const FusedParams& p, int t) const
     {
         return p.mode == kModeReduceScatter ? t / p.n_shards : t;
@@ -109,7 +120,40 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     sc.unit = cid / PAIR;
     sc.n_units = p.n_consumers / PAIR;
     sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb * (p.mode == kModeReduceScatter ? p.n_shards : 1);
+    sc.dyn = PAIR == 1 && p.dyn;
     return sc;
+}
+
+// Dynamic schedule: wait (bounded) until the scheduler has published ring
+// entry k.  Returns false on a pipeline timeout.
+template <int PAIR>
+__device__ __forceinline__ bool ring_wait(const FusedParams& p, const ConsumerSmem<PAIR>& s, int k)
+{
+    if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+            record_error(p.ctrl, kErrTimeout);
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
+// The k-th tile of this unit (k counts from 0): u + k * n_units statically,
+// or ring entry k.  Returns false when the unit has no k-th tile.
+template <int PAIR>
+__device__ __forceinline__ bool kth_tile(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                         int k, int& t)
+{
+    if (!sc.dyn) {
+        t = sc.unit + k * sc.n_units;
+        return t < sc.n_tiles;
+    }
+    if (!ring_wait<PAIR>(p, s, k)) return false;
+    t = s.ring[k % kRing];
+    return t >= 0;
 }
 
 // Gate: the rows of row block mb, K-slice s, are complete this round.
@@ -137,13 +181,56 @@ __device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb,
 // the TMA warp with a CTA-scope release of the running count.  A gate that
 // times out is handed on as well, so the pipeline drains; the status word
 // holds the error.
+// Dynamic schedule (role switch): the gate warp is also the CTA's scheduler.
+// It takes the next tile from the round's ticket counter when the TMA warp
+// has issued every load of the current one -- the moment the pipeline needs
+// it, so no CTA holds a tile another could start sooner -- publishes it in
+// the ring (CTA-scope release) and then waits for that tile's gates.  A ring
+// entry is reused only after the epilogue warps have started its tile.  A
+// ticket past the last tile publishes -1 and ends every role.
+template <int PAIR>
+__device__ int sched_next(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc, int k)
+{
+    const uint32_t lane = ptx::lane_id();
+    int t = -1;
+    if (lane == 0) {
+        bool room = true;
+        const int need_epi = k >= kRing ? kEpiWarps * (k - kRing + 1) : 0;
+        const uint64_t start = ptx::globaltimer();
+        for (uint32_t i = 1; ptx::ld_acquire_cta_smem(s.tma_done) < k ||
+                             ptx::ld_acquire_cta_smem(s.epi_started) < need_epi; ++i) {
+            if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+                record_error(p.ctrl, kErrTimeout);
+                room = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+        if (room) {
+            t = ptx::atom_add_relaxed_gpu(p.ctrl.work, 1);
+            if (t >= sc.n_tiles) t = -1;
+        }
+        s.ring[k % kRing] = t;
+        ptx::st_release_cta_smem(s.ring_head, k + 1);
+    }
+    return __shfl_sync(0xffffffffu, t, 0);
+}
+
 template <int PAIR>
 __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
 {
     const uint32_t lane = ptx::lane_id();
     unsigned long long polls = 0;
     int passed = 0;
-    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
+    for (int k = 0;; ++k) {
+        int t;
+        if (sc.dyn) {
+            t = sched_next<PAIR>(p, s, sc, k);
+            if (t < 0) break;
+            if (!p.gated) continue;
+        } else if (!kth_tile<PAIR>(p, s, sc, k, t)) {
+            break;
+        }
         const int mb = sc.row_block(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl) {
             polls += gate(p, mb, sl);
@@ -164,19 +251,40 @@ __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s,
 // free, and the stage's A box follows once the slice's gate has passed.
 template <int PAIR>
 struct BCursor {
+    int k;                    // index of the cursor's tile in this unit's schedule
     int t, kb, brow, n0;      // next k-block to load: tile, k-block, B row base, B column base
+    bool have;                // t is known (a dynamic schedule publishes tiles as it goes)
     int issued;               // stages armed so far
     uint32_t stage, phase;
 };
 
+// Resolve the cursor's tile: 1 = known (t >= n_tiles: no more tiles), 0 = not
+// published yet (only without `block`), -1 = pipeline timeout.
 template <int PAIR>
-__device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR>& sc, BCursor<PAIR>& b)
+__device__ __forceinline__ int b_resolve(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                         BCursor<PAIR>& b, bool block)
 {
-    if (b.t >= sc.n_tiles) return;
-    const int mb = sc.row_block(p, b.t);
-    b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
-           : (p.mode == kModeReduceScatter) ? sc.shard(p, b.t) * p.K : 0;
-    b.n0 = sc.col_block(p, b.t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+    if (b.have) return 1;
+    int t;
+    if (!sc.dyn) {
+        t = sc.unit + b.k * sc.n_units;
+    } else {
+        if (ptx::ld_acquire_cta_smem(s.ring_head) <= b.k) {
+            if (!block) return 0;
+            if (!ring_wait<PAIR>(p, s, b.k)) return -1;
+        }
+        t = s.ring[b.k % kRing];
+        if (t < 0) t = sc.n_tiles;
+    }
+    b.t = t;
+    b.have = true;
+    if (t < sc.n_tiles) {
+        const int mb = sc.row_block(p, t);
+        b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
+               : (p.mode == kModeReduceScatter) ? sc.shard(p, t) * p.K : 0;
+        b.n0 = sc.col_block(p, t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+    }
+    return 1;
 }
 
 // Arm the cursor's stage and issue its B boxes (the stage must be free).
@@ -207,18 +315,22 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
     }
     if (++b.kb == p.n_kb) {
         b.kb = 0;
-        b.t += sc.n_units;
-        b_tile<PAIR>(p, sc, b);
+        ++b.k;
+        b.have = false;
     }
 }
 
-// Arm stages until the cursor is `ahead` stages past `a_count` (blocking on
-// free stages only when `block`).  Returns false on a pipeline timeout.
+// Arm stages until the cursor has armed `upto` stages (blocking on free
+// stages and unpublished tiles only when `block`).  Returns false on a
+// pipeline timeout.
 template <int PAIR>
 __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                       BCursor<PAIR>& b, int upto, bool block)
 {
-    while (b.issued < upto && b.t < sc.n_tiles) {
+    while (b.issued < upto) {
+        const int r = b_resolve<PAIR>(p, s, sc, b, block);
+        if (r < 0) return false;
+        if (r == 0 || b.t >= sc.n_tiles) return true;
         if (block) {
             if (!mbar_wait(&s.empty[b.stage], b.phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return false;
         } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
@@ -258,16 +370,19 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     using T = Tile<PAIR>;
     if (ptx::lane_id() != 0) return;
     BCursor<PAIR> b;
-    b.t = sc.unit;
+    b.k = 0;
+    b.t = 0;
     b.kb = 0;
+    b.have = false;
     b.issued = 0;
     b.stage = 0;
     b.phase = 0;
-    b_tile<PAIR>(p, sc, b);
     uint32_t stage = 0;
     int a_count = 0;
     int gate_idx = 0;
-    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
+    for (int k = 0;; ++k) {
+        int t;
+        if (!kth_tile<PAIR>(p, s, sc, k, t)) break;
         const int arow = sc.a_row(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
@@ -291,6 +406,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 if (++stage == T::kStages) stage = 0;
             }
         }
+        if (sc.dyn) ptx::st_release_cta_smem(s.tma_done, k + 1);
     }
 }
 
@@ -302,8 +418,9 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     using T = Tile<PAIR>;
     if (ptx::lane_id() != 0 || sc.rank != 0) return;
     uint32_t stage = 0, phase = 0;
-    int local = 0;
-    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
+    for (int local = 0;; ++local) {
+        int t;
+        if (!kth_tile<PAIR>(p, s, sc, local, t)) break;
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
@@ -358,8 +475,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
-    int local = 0;
-    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
+    for (int local = 0;; ++local) {
+        int t;
+        if (!__all_sync(0xffffffffu, kth_tile<PAIR>(p, s, sc, local, t))) break;
+        // the ring entry is read: the scheduler may reuse it kRing tiles on
+        if (sc.dyn && lane == 0) ptx::red_add_release_cta_smem(s.epi_started, 1);
         const int arow = sc.a_row(p, t);
         const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
@@ -452,6 +572,9 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
             ptx::mbar_init(&s.tempty[i], kEpiWarps * PAIR);
         }
         *s.gates_passed = 0;
+        *s.ring_head = 0;
+        *s.epi_started = 0;
+        *s.tma_done = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
         ptx::prefetch_tmap(&p.tmap_b);
@@ -482,7 +605,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     if (warp == 0) consumer_tma<PAIR>(p, s, sc);
     else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
     else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
-    else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
+    else if (warp == kGateWarp && (p.gated || sc.dyn)) consumer_gate<PAIR>(p, s, sc);
     __syncwarp();
 
     // teardown: every role of both CTAs has finished before TMEM is freed

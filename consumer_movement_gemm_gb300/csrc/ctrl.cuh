@@ -150,6 +150,8 @@ struct FusedParams {
     int rs_tiles;         // partial tiles: S x output tiles; tile t publishes counter t
     int rs_pair;          // rows of an output tile / 128
     int rs_join;          // consumers take reduction items once their tiles are done (role switch)
+    int dyn;              // consumer tiles handed out by a ticket counter (ctrl.work, zeroed by the plan kernel)
+    int join;             // producer CTAs become consumers once their copies are done (role switch)
     void* rs_out;         // [M][N] bf16
     // destinations
     void* gathered;       // gathered / dispatched buffer
@@ -170,6 +172,7 @@ struct PlanParams {
     int* expert_offsets;  // caller-visible [E+1]
     Plan plan;
     int* status;
+    int* work;            // ticket counter of the fused kernel that follows (zeroed here)
 };
 
 struct CopyParams {

@@ -36,8 +36,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    if (static_cast<int>(blockIdx.x) < p.n_producers) producer(p, smem, blockIdx.x);
-    else consumer<PAIR>(p, smem, blockIdx.x - p.n_producers);
+    if (static_cast<int>(blockIdx.x) < p.n_producers) {
+        producer(p, smem, blockIdx.x);
+        // role switch: with its copies done, the producer CTA takes GEMM tiles
+        // from the round's ticket counter like any consumer
+        if (p.join) consumer<PAIR>(p, smem, -1);
+    } else {
+        consumer<PAIR>(p, smem, blockIdx.x - p.n_producers);
+    }
 }
 
 cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool cooperative, int pair, bool pdl)

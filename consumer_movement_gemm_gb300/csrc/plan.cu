@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();         // the fused kernel may start its launch and prologue
     const int tid = threadIdx.x;
+    if (tid == 0 && p.work) *p.work = 0;   // the fused kernel's tile tickets start at 0
     const int* meta_in = p.plan.meta;
     if (tid == 0) {
         s_zero = p.force_zero;

@@ -309,6 +309,10 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
         if (lane == 0 && st.n > 0) item_done(p, st.counter, st.n);
         __syncwarp();
     }
+    // every load this warp issued has completed; the barrier's memory may be
+    // reused (a producer CTA that turns consumer)
+    if (lane == 0) ptx::mbar_inval(bar);
+    __syncwarp();
 }
 
 // Reduce-scatter reduction.  An item is 16 rows x 256 columns of one output

@@ -101,6 +101,11 @@ __device__ __forceinline__ void st_release_cta_smem(int* p, int v)
     asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_add_release_cta_smem(int* p, int v)
+{
+    asm volatile("red.release.cta.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int ld_acquire_cta_smem(const int* p)
 {
     int v;
@@ -173,6 +178,12 @@ __device__ __forceinline__ void grid_dep_launch()
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Retire an mbarrier before its shared memory is used for anything else.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void fence_mbar_init()

@@ -334,7 +334,13 @@ static void base_params(tovl_ctx* h, FusedParams& p)
 // With CTA pairs (pair = 2) a consumer unit is two CTAs computing 256-row
 // tiles, both counts are even, and the grid is limited to the pairs that can
 // be co-resident.
-static void split_ctas(tovl_ctx* h, int& P, int& C, int n_mb, int n_nb, double copy_bytes, double flops, int pair)
+// With `joining` producers (they turn consumer once their copies are done),
+// the copy only has to stay ahead of the GEMM: any P above the balance point
+// gives about the same total, and a margin opens the gates sooner, so P is
+// twice the balance point (measured on the dispatch workloads: flat between
+// 1.5x and 3x) and the wave rule does not apply.
+static void split_ctas(tovl_ctx* h, int& P, int& C, int n_mb, int n_nb, double copy_bytes, double flops, int pair,
+                       bool joining = false)
 {
     int S = h->num_sms;
     if (pair == 2 && 2 * h->max_pairs < S) S = 2 * h->max_pairs;
@@ -344,9 +350,10 @@ static void split_ctas(tovl_ctx* h, int& P, int& C, int n_mb, int n_nb, double c
     } else {
         const double tc = copy_bytes / 60e9, tg = flops / 10e12;
         int p = static_cast<int>(S * tc / (tc + tg + 1e-30) + 0.5);
-        const int pmax = S / 4;
+        const int pmax = joining ? S / 2 : S / 4;
+        if (joining) p *= 2;
         p = p < 4 ? 4 : (p > pmax ? pmax : p);
-        if (tiles > 0) {
+        if (tiles > 0 && !joining) {
             const int units = (S - p) / pair;
             const long long waves = (tiles + units - 1) / units;
             const int cmin = static_cast<int>((tiles + waves - 1) / waves) * pair;
@@ -563,6 +570,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     pp.expert_offsets = expert_offsets;
     pp.plan = h->plan;
     pp.status = h->ctrl.status;
+    pp.work = h->ctrl.work;
     cudaError_t e = launch_plan(pp, s, h->pdl && h->pdl_ok);
     if (e != cudaSuccess && h->pdl && h->pdl_ok) {
         cudaGetLastError();
@@ -582,10 +590,14 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.row_bytes = H * 2;
     int P, C;
     split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
-               2.0 * pairs * static_cast<double>(N) * H, 1);
+               2.0 * pairs * static_cast<double>(N) * H, 1, h->role_switch);
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 1;
+    // role switch: consumer tiles come from the ticket counter (zeroed by the
+    // plan kernel) and producer CTAs take tiles once their copies are done
+    p.dyn = h->role_switch ? 1 : 0;
+    p.join = h->role_switch ? 1 : 0;
     call_geometry(h, p, C, 1);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;

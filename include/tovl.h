@@ -284,10 +284,12 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * kernel before it -- plan counting, plan finalisation, the fused kernel,
  * combine -- and every kernel waits for its predecessor before it reads
  * memory; 0 = plain stream order; reads back 0 if the device refused it),
- * 16 = role switch in tovl_gemm_reduce_scatter (1, the default: consumer
- * CTAs that have finished their partial tiles take reduction items, handed
- * out by a ticket counter, beside the producer CTAs; 0 = producers reduce
- * alone),
+ * 16 = role switch (1, the default; 0 = fixed roles): in
+ * tovl_dispatch_grouped_gemm consumer tiles are handed out by a ticket
+ * counter and producer CTAs take tiles once their copies are done (the
+ * automatic split then gives the copy twice its balance share); in
+ * tovl_gemm_reduce_scatter consumer CTAs that have finished their partial
+ * tiles take reduction items beside the producer CTAs,
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

@@ -201,11 +201,14 @@ ROUTINGS = {
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
 @pytest.mark.parametrize("k_slices", [1, 2])
-@pytest.mark.parametrize("mode", [0, 1])
-def test_dispatch_grouped_gemm_small(routing, k_slices, mode):
+@pytest.mark.parametrize("mode,switch", [(0, 1), (1, 1), (0, 0)])
+def test_dispatch_grouped_gemm_small(routing, k_slices, mode, switch):
+    # switch: tiles from the ticket counter and producer CTAs that turn
+    # consumer (1), or the static schedule (0)
     H, N = 192, 256
     with _handle(k_slices=k_slices) as h:
         h.set_option(tovl.OPT_PRODUCER_MODE, mode)
+        h.set_option(tovl.OPT_ROLE_SWITCH, switch)
         for r in range(1, 4):
             topk_np, E = ROUTINGS[routing](workloads.round_seed(1, r))
             T = topk_np.shape[0]
