@@ -53,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip the extra workloads")
     ap.add_argument("--full", action="store_true", help="extra workloads at their full round counts")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["fused", "gemm", "copy", "dispatch"], default=None,
+    ap.add_argument("--profile", choices=["fused", "gemm", "copy", "dispatch", "combine", "rs"], default=None,
                     help="run only W + K calls of one kernel on a small case (for ncu captures) and exit")
     ap.add_argument("--no-coop", action="store_true",
                     help="launch fused kernels without the cooperative attribute (profiler replay)")
@@ -500,6 +500,8 @@ def run_tovl(args):
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     h = tovl.Handle(local, max_rows=1 << 14, producer_ctas=args.producers, k_slices=args.k_slices)
+    if args.no_coop:
+        h.set_option(tovl.OPT_COOPERATIVE, 0)   # for profilers that cannot replay cooperative cluster launches
     X, W, gathered, out = tp_setup(h, cfg, dev)
     timer = Timer(stream)
     step = lambda: h.gather_gemm(X, W, gathered, out, stream=stream)  # noqa: E731
@@ -589,7 +591,9 @@ def run_profile(args):
       fused     tovl_gather_gemm on the TP shape (about 110 MB resident)
       gemm      tovl_gemm_only on the TP shape
       copy      tovl_gated_copy, 2^18 rows x 8 KB, gated (4 GB resident)
-      dispatch  tovl_dispatch_grouped_gemm on the uniform top-2 workload"""
+      dispatch  tovl_dispatch_grouped_gemm on the uniform top-2 workload
+      combine   the dispatch calls, each followed by tovl_combine
+      rs        tovl_gemm_reduce_scatter on the TP shape split four ways along K"""
     import torch
     import workloads
     from consumer_movement_gemm_gb300 import build as tovl_build
@@ -618,6 +622,19 @@ def run_profile(args):
             for _ in range(n):
                 h.gated_copy(src, dst, perm, gated=True)
             assert h.sync_status() == 0
+    elif args.profile == "rs":
+        cfg = workloads.TP
+        S, M, K, N = cfg.shards, cfg.M, cfg.K, cfg.N
+        X = workloads.bf16_normal((S, M, K // S), 1 / K ** 0.5, 0, dev)
+        W = workloads.bf16_normal((S, K // S, N), 1 / K ** 0.5, 1, dev)
+        partials = torch.empty(S, M, N, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        with tovl.Handle(0, max_rows=1 << 14, k_slices=4) as h:
+            if args.no_coop:
+                h.set_option(tovl.OPT_COOPERATIVE, 0)
+            for _ in range(n):
+                h.gemm_reduce_scatter(X, W, partials, out)
+            assert h.sync_status() == 0
     else:
         cfg = workloads.DISPATCH
         x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
@@ -629,8 +646,13 @@ def run_profile(args):
             dispatched = torch.zeros(rows, cfg.H, dtype=torch.bfloat16, device=dev)
             offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
             out = torch.empty(rows, cfg.N, dtype=torch.bfloat16, device=dev)
+            w = torch.from_numpy(workloads.gate_weights(cfg.T, cfg.k, 0)).to(dev)
+            staging = torch.empty(cfg.T * cfg.k, cfg.N, dtype=torch.bfloat16, device=dev)
+            combined = torch.empty(cfg.T, cfg.N, dtype=torch.bfloat16, device=dev)
             for _ in range(n):
                 h.dispatch_grouped_gemm(x, topk, W, dispatched, offs, out)
+                if args.profile == "combine":
+                    h.combine(out, w, staging, combined)
             assert h.sync_status() == 0
     torch.cuda.synchronize()
     print(json.dumps({"profile": args.profile, "calls": n}))
