@@ -124,38 +124,6 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     return sc;
 }
 
-// Dynamic schedule: wait (bounded) until the scheduler has published ring
-// entry k.  Returns false on a pipeline timeout.
-template <int PAIR>
-__device__ __forceinline__ bool ring_wait(const FusedParams& p, const ConsumerSmem<PAIR>& s, int k)
-{
-    if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
-    const uint64_t start = ptx::globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
-        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
-            record_error(p.ctrl, kErrTimeout);
-            return false;
-        }
-        __nanosleep(32);
-    }
-}
-
-// The k-th tile of this unit (k counts from 0): u + k * n_units statically,
-// or ring entry k.  Returns false when the unit has no k-th tile.
-template <int PAIR>
-__device__ __forceinline__ bool kth_tile(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
-                                         int k, int& t)
-{
-    if (!sc.dyn) {
-        t = sc.unit + k * sc.n_units;
-        return t < sc.n_tiles;
-    }
-    if (!ring_wait<PAIR>(p, s, k)) return false;
-    t = s.ring[k % kRing];
-    return t >= 0;
-}
-
 // Gate: the rows of row block mb, K-slice s, are complete this round.
 __device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb, int s)
 {
@@ -181,56 +149,13 @@ __device__ __forceinline__ unsigned long long gate(const FusedParams& p, int mb,
 // the TMA warp with a CTA-scope release of the running count.  A gate that
 // times out is handed on as well, so the pipeline drains; the status word
 // holds the error.
-// Dynamic schedule (role switch): the gate warp is also the CTA's scheduler.
-// It takes the next tile from the round's ticket counter when the TMA warp
-// has issued every load of the current one -- the moment the pipeline needs
-// it, so no CTA holds a tile another could start sooner -- publishes it in
-// the ring (CTA-scope release) and then waits for that tile's gates.  A ring
-// entry is reused only after the epilogue warps have started its tile.  A
-// ticket past the last tile publishes -1 and ends every role.
-template <int PAIR>
-__device__ int sched_next(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc, int k)
-{
-    const uint32_t lane = ptx::lane_id();
-    int t = -1;
-    if (lane == 0) {
-        bool room = true;
-        const int need_epi = k >= kRing ? kEpiWarps * (k - kRing + 1) : 0;
-        const uint64_t start = ptx::globaltimer();
-        for (uint32_t i = 1; ptx::ld_acquire_cta_smem(s.tma_done) < k ||
-                             ptx::ld_acquire_cta_smem(s.epi_started) < need_epi; ++i) {
-            if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
-                record_error(p.ctrl, kErrTimeout);
-                room = false;
-                break;
-            }
-            __nanosleep(32);
-        }
-        if (room) {
-            t = ptx::atom_add_relaxed_gpu(p.ctrl.work, 1);
-            if (t >= sc.n_tiles) t = -1;
-        }
-        s.ring[k % kRing] = t;
-        ptx::st_release_cta_smem(s.ring_head, k + 1);
-    }
-    return __shfl_sync(0xffffffffu, t, 0);
-}
-
 template <int PAIR>
 __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
 {
     const uint32_t lane = ptx::lane_id();
     unsigned long long polls = 0;
     int passed = 0;
-    for (int k = 0;; ++k) {
-        int t;
-        if (sc.dyn) {
-            t = sched_next<PAIR>(p, s, sc, k);
-            if (t < 0) break;
-            if (!p.gated) continue;
-        } else if (!kth_tile<PAIR>(p, s, sc, k, t)) {
-            break;
-        }
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
         const int mb = sc.row_block(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl) {
             polls += gate(p, mb, sl);
@@ -251,40 +176,19 @@ __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s,
 // free, and the stage's A box follows once the slice's gate has passed.
 template <int PAIR>
 struct BCursor {
-    int k;                    // index of the cursor's tile in this unit's schedule
     int t, kb, brow, n0;      // next k-block to load: tile, k-block, B row base, B column base
-    bool have;                // t is known (a dynamic schedule publishes tiles as it goes)
     int issued;               // stages armed so far
     uint32_t stage, phase;
 };
 
-// Resolve the cursor's tile: 1 = known (t >= n_tiles: no more tiles), 0 = not
-// published yet (only without `block`), -1 = pipeline timeout.
 template <int PAIR>
-__device__ __forceinline__ int b_resolve(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
-                                         BCursor<PAIR>& b, bool block)
+__device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR>& sc, BCursor<PAIR>& b)
 {
-    if (b.have) return 1;
-    int t;
-    if (!sc.dyn) {
-        t = sc.unit + b.k * sc.n_units;
-    } else {
-        if (ptx::ld_acquire_cta_smem(s.ring_head) <= b.k) {
-            if (!block) return 0;
-            if (!ring_wait<PAIR>(p, s, b.k)) return -1;
-        }
-        t = s.ring[b.k % kRing];
-        if (t < 0) t = sc.n_tiles;
-    }
-    b.t = t;
-    b.have = true;
-    if (t < sc.n_tiles) {
-        const int mb = sc.row_block(p, t);
-        b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
-               : (p.mode == kModeReduceScatter) ? sc.shard(p, t) * p.K : 0;
-        b.n0 = sc.col_block(p, t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
-    }
-    return 1;
+    if (b.t >= sc.n_tiles) return;
+    const int mb = sc.row_block(p, b.t);
+    b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
+           : (p.mode == kModeReduceScatter) ? sc.shard(p, b.t) * p.K : 0;
+    b.n0 = sc.col_block(p, b.t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
 }
 
 // Arm the cursor's stage and issue its B boxes (the stage must be free).
@@ -315,22 +219,18 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
     }
     if (++b.kb == p.n_kb) {
         b.kb = 0;
-        ++b.k;
-        b.have = false;
+        b.t += sc.n_units;
+        b_tile<PAIR>(p, sc, b);
     }
 }
 
-// Arm stages until the cursor has armed `upto` stages (blocking on free
-// stages and unpublished tiles only when `block`).  Returns false on a
-// pipeline timeout.
+// Arm stages until the cursor is `ahead` stages past `a_count` (blocking on
+// free stages only when `block`).  Returns false on a pipeline timeout.
 template <int PAIR>
 __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                       BCursor<PAIR>& b, int upto, bool block)
 {
-    while (b.issued < upto) {
-        const int r = b_resolve<PAIR>(p, s, sc, b, block);
-        if (r < 0) return false;
-        if (r == 0 || b.t >= sc.n_tiles) return true;
+    while (b.issued < upto && b.t < sc.n_tiles) {
         if (block) {
             if (!mbar_wait(&s.empty[b.stage], b.phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return false;
         } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
@@ -370,19 +270,16 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     using T = Tile<PAIR>;
     if (ptx::lane_id() != 0) return;
     BCursor<PAIR> b;
-    b.k = 0;
-    b.t = 0;
+    b.t = sc.unit;
     b.kb = 0;
-    b.have = false;
     b.issued = 0;
     b.stage = 0;
     b.phase = 0;
+    b_tile<PAIR>(p, sc, b);
     uint32_t stage = 0;
     int a_count = 0;
     int gate_idx = 0;
-    for (int k = 0;; ++k) {
-        int t;
-        if (!kth_tile<PAIR>(p, s, sc, k, t)) break;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
         const int arow = sc.a_row(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
@@ -406,7 +303,6 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 if (++stage == T::kStages) stage = 0;
             }
         }
-        if (sc.dyn) ptx::st_release_cta_smem(s.tma_done, k + 1);
     }
 }
 
@@ -418,9 +314,8 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     using T = Tile<PAIR>;
     if (ptx::lane_id() != 0 || sc.rank != 0) return;
     uint32_t stage = 0, phase = 0;
-    for (int local = 0;; ++local) {
-        int t;
-        if (!kth_tile<PAIR>(p, s, sc, local, t)) break;
+    int local = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
@@ -475,11 +370,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
-    for (int local = 0;; ++local) {
-        int t;
-        if (!__all_sync(0xffffffffu, kth_tile<PAIR>(p, s, sc, local, t))) break;
-        // the ring entry is read: the scheduler may reuse it kRing tiles on
-        if (sc.dyn && lane == 0) ptx::red_add_release_cta_smem(s.epi_started, 1);
+    int local = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const int arow = sc.a_row(p, t);
         const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
@@ -556,6 +448,423 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     __syncwarp();
 }
 
+// Role switch, dynamic schedule (single-CTA tiles): the same roles as above,
+// with tiles taken from the round's ticket counter through a shared-memory
+// ring instead of a fixed stride.  Kept apart from the fixed-schedule roles so
+// those compile exactly as they are.
+namespace dyn {
+
+// Dynamic schedule: wait (bounded) until the scheduler has published ring
+// entry k.  Returns false on a pipeline timeout.
+template <int PAIR>
+__device__ __forceinline__ bool ring_wait(const FusedParams& p, const ConsumerSmem<PAIR>& s, int k)
+{
+    if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+            record_error(p.ctrl, kErrTimeout);
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
+// The k-th tile of this unit (k counts from 0): u + k * n_units statically,
+// or ring entry k.  Returns false when the unit has no k-th tile.
+template <int PAIR, bool DYN>
+__device__ __forceinline__ bool kth_tile(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                         int k, int& t)
+{
+    if constexpr (!DYN) {
+        t = sc.unit + k * sc.n_units;
+        return t < sc.n_tiles;
+    }
+    if (!ring_wait<PAIR>(p, s, k)) return false;
+    t = s.ring[k % kRing];
+    return t >= 0;
+}
+
+// Dynamic schedule (role switch): the gate warp is also the CTA's scheduler.
+// It takes the next tile from the round's ticket counter when the TMA warp
+// has issued every load of the current one -- the moment the pipeline needs
+// it, so no CTA holds a tile another could start sooner -- publishes it in
+// the ring (CTA-scope release) and then waits for that tile's gates.  A ring
+// entry is reused only after the epilogue warps have started its tile.  A
+// ticket past the last tile publishes -1 and ends every role.
+template <int PAIR>
+__device__ int sched_next(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc, int k)
+{
+    const uint32_t lane = ptx::lane_id();
+    int t = -1;
+    if (lane == 0) {
+        bool room = true;
+        const int need_epi = k >= kRing ? kEpiWarps * (k - kRing + 1) : 0;
+        const uint64_t start = ptx::globaltimer();
+        for (uint32_t i = 1; ptx::ld_acquire_cta_smem(s.tma_done) < k ||
+                             ptx::ld_acquire_cta_smem(s.epi_started) < need_epi; ++i) {
+            if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+                record_error(p.ctrl, kErrTimeout);
+                room = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+        if (room) {
+            t = ptx::atom_add_relaxed_gpu(p.ctrl.work, 1);
+            if (t >= sc.n_tiles) t = -1;
+        }
+        s.ring[k % kRing] = t;
+        ptx::st_release_cta_smem(s.ring_head, k + 1);
+    }
+    return __shfl_sync(0xffffffffu, t, 0);
+}
+
+template <int PAIR, bool DYN>
+__device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
+{
+    const uint32_t lane = ptx::lane_id();
+    unsigned long long polls = 0;
+    int passed = 0;
+    for (int k = 0;; ++k) {
+        int t;
+        if constexpr (DYN) {
+            t = sched_next<PAIR>(p, s, sc, k);
+            if (t < 0) break;
+            if (!p.gated) continue;
+        } else if (!kth_tile<PAIR, DYN>(p, s, sc, k, t)) {
+            break;
+        }
+        const int mb = sc.row_block(p, t);
+        for (int sl = 0; sl < p.k_slices; ++sl) {
+            polls += gate(p, mb, sl);
+            ++passed;
+            if (lane == 0) {
+                ptx::st_release_cta_smem(s.gates_passed, passed);
+                trace_put(p, static_cast<long long>(t) * p.k_slices + sl, ptx::globaltimer());
+            }
+            __syncwarp();
+        }
+    }
+    if (p.stats && lane == 0 && polls) atomicAdd(p.ctrl.stats + kStatGatePolls, polls);
+}
+
+// Weight (B) cursor of the TMA lane.  B does not depend on the producers, so
+// its k-blocks are loaded ahead of the gate: a stage's B boxes are issued (and
+// the stage's full barrier armed for A + B bytes) as soon as the stage is
+// free, and the stage's A box follows once the slice's gate has passed.
+template <int PAIR>
+struct BCursor {
+    int k;                    // index of the cursor's tile in this unit's schedule
+    int t, kb, brow, n0;      // next k-block to load: tile, k-block, B row base, B column base
+    bool have;                // t is known (a dynamic schedule publishes tiles as it goes)
+    int issued;               // stages armed so far
+    uint32_t stage, phase;
+};
+
+// Resolve the cursor's tile: 1 = known (t >= n_tiles: no more tiles), 0 = not
+// published yet (only without `block`), -1 = pipeline timeout.
+template <int PAIR, bool DYN>
+__device__ __forceinline__ int b_resolve(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                         BCursor<PAIR>& b, bool block)
+{
+    if (b.have) return 1;
+    int t;
+    if constexpr (!DYN) {
+        t = sc.unit + b.k * sc.n_units;
+    } else {
+        if (ptx::ld_acquire_cta_smem(s.ring_head) <= b.k) {
+            if (!block) return 0;
+            if (!ring_wait<PAIR>(p, s, b.k)) return -1;
+        }
+        t = s.ring[b.k % kRing];
+        if (t < 0) t = sc.n_tiles;
+    }
+    b.t = t;
+    b.have = true;
+    if (t < sc.n_tiles) {
+        const int mb = sc.row_block(p, t);
+        b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
+               : (p.mode == kModeReduceScatter) ? sc.shard(p, t) * p.K : 0;
+        b.n0 = sc.col_block(p, t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+    }
+    return 1;
+}
+
+// Arm the cursor's stage and issue its B boxes (the stage must be free).
+template <int PAIR, bool DYN>
+__device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                        BCursor<PAIR>& b)
+{
+    using T = Tile<PAIR>;
+    uint8_t* bdst = s.b + b.stage * T::kStageB;
+    if (PAIR == 1) {
+        ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
+#pragma unroll
+        for (int j = 0; j < T::kBBoxes; ++j)
+            ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
+                             b.brow + b.kb * kTileK);
+    } else {
+        // both CTAs' bytes are counted on the first CTA's barrier
+        if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
+        const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
+#pragma unroll
+        for (int j = 0; j < T::kBBoxes; ++j)
+            ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64, b.brow + b.kb * kTileK);
+    }
+    ++b.issued;
+    if (++b.stage == T::kStages) {
+        b.stage = 0;
+        b.phase ^= 1u;
+    }
+    if (++b.kb == p.n_kb) {
+        b.kb = 0;
+        ++b.k;
+        b.have = false;
+        // a fixed schedule knows the next tile: resolve it at once
+        if constexpr (!DYN) b_resolve<PAIR, DYN>(p, s, sc, b, false);
+    }
+}
+
+// Arm stages until the cursor has armed `upto` stages (blocking on free
+// stages and unpublished tiles only when `block`).  Returns false on a
+// pipeline timeout.
+template <int PAIR, bool DYN>
+__device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                      BCursor<PAIR>& b, int upto, bool block)
+{
+    while (b.issued < upto) {
+        const int r = b_resolve<PAIR, DYN>(p, s, sc, b, block);
+        if (r < 0) return false;
+        if (r == 0 || b.t >= sc.n_tiles) return true;
+        if (block) {
+            if (!mbar_wait(&s.empty[b.stage], b.phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return false;
+        } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
+            return true;
+        }
+        b_issue<PAIR, DYN>(p, s, sc, b);
+    }
+    return true;
+}
+
+// TMA lane: wait until the gate warp has passed gate number `idx` (bounded),
+// arming free stages with B meanwhile.
+template <int PAIR, bool DYN>
+__device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                          BCursor<PAIR>& b, int a_count, int idx)
+{
+    using T = Tile<PAIR>;
+    if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (!b_run<PAIR, DYN>(p, s, sc, b, a_count + T::kStages, false)) return false;
+        if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
+        if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
+            record_error(p.ctrl, kErrTimeout);
+            return false;
+        }
+        __nanosleep(20);
+    }
+}
+
+// TMA warp: per tile and K-slice, wait for the slice's gate, then stream the
+// slice's A k-blocks into stages whose B the cursor above has already
+// loaded.  One lane issues everything.
+template <int PAIR, bool DYN>
+__device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
+{
+    using T = Tile<PAIR>;
+    if (ptx::lane_id() != 0) return;
+    BCursor<PAIR> b;
+    b.k = 0;
+    b.t = 0;
+    b.kb = 0;
+    b.have = false;
+    b.issued = 0;
+    b.stage = 0;
+    b.phase = 0;
+    uint32_t stage = 0;
+    int a_count = 0;
+    int gate_idx = 0;
+    for (int k = 0;; ++k) {
+        int t;
+        if (!kth_tile<PAIR, DYN>(p, s, sc, k, t)) break;
+        const int arow = sc.a_row(p, t);
+        for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
+            if (p.gated) {
+                if (!wait_gate<PAIR, DYN>(p, s, sc, b, a_count, gate_idx)) return;
+                // the rows were written through the generic proxy; order them
+                // before this thread's tensor-memory-access (async proxy) reads
+                ptx::fence_proxy_async_global();
+            }
+            const int kb1 = kb_begin(p, sl + 1);
+            for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
+                // this k-block's stage is armed and holds (or receives) its B
+                if (!b_run<PAIR, DYN>(p, s, sc, b, a_count + 1, true)) return;
+                uint8_t* adst = s.a + stage * T::kStageA;
+                if (PAIR == 1) {
+                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow);
+                } else {
+                    const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
+                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, arow);
+                }
+                ++a_count;
+                if (++stage == T::kStages) stage = 0;
+            }
+        }
+        if constexpr (DYN) ptx::st_release_cta_smem(s.tma_done, k + 1);
+    }
+}
+
+// MMA warp: one lane (of the pair's first CTA) issues the MMAs.
+template <int PAIR, bool DYN>
+__device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                             uint32_t tmem_base)
+{
+    using T = Tile<PAIR>;
+    if (ptx::lane_id() != 0 || sc.rank != 0) return;
+    uint32_t stage = 0, phase = 0;
+    for (int local = 0;; ++local) {
+        int t;
+        if (!kth_tile<PAIR, DYN>(p, s, sc, local, t)) break;
+        const uint32_t acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + acc * kTileN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+            if (!mbar_wait(&s.full[stage], phase, p.ctrl, p.pipe_timeout_ns)) return;
+            ptx::tc_fence_after();
+            const uint32_t a0 = ptx::smem_u32(s.a + stage * T::kStageA);
+            const uint32_t b0 = ptx::smem_u32(s.b + stage * T::kStageB);
+#pragma unroll
+            for (int k = 0; k < kTileK / kUmmaK; ++k) {
+                // A: K-major, 128B swizzle; +32 B per 16-element k step inside
+                //    the swizzle row; 8-row groups 1024 B apart.
+                const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
+                // B: MN-major, 128B swizzle; +2048 B per 16 k-rows; 8-k-row
+                //    groups 1024 B apart; 64-column blocks 8 KB apart.
+                const uint64_t bd = ptx::smem_desc_sw128(b0 + k * 2048, kTileK * 128, 1024);
+                if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                else ptx::umma_bf16_pair(d, ad, bd, T::kIdesc, (kb | k) != 0);
+            }
+            if (PAIR == 1) ptx::umma_commit(&s.empty[stage]);
+            else ptx::umma_commit_pair(&s.empty[stage], 0x3);
+            if (++stage == T::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (PAIR == 1) ptx::umma_commit(&s.tfull[acc]);
+        else ptx::umma_commit_pair(&s.tfull[acc], 0x3);
+    }
+}
+
+// Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) ->
+// shared memory -> TMA tensor store.  Warp w reads TMEM lane quarter w % 4
+// (the quarter its position allows), i.e. 32 output rows, and one half of
+// the 256 accumulator columns, as four 32 x 32 boxes.  A box is written into
+// the warp's 2 KB buffer in the 64-byte swizzled layout the store's tensor
+// map expects (16-byte chunk j of 64-byte row r at chunk j ^ ((r / 2) % 4):
+// the eight rows a quarter-warp writes hit distinct banks), then one lane
+// stores it; rows past the output's extent (the ragged tail of M) are
+// clipped by the store.  The accumulator is released as soon as its last
+// columns are in registers.
+template <int PAIR, bool DYN>
+__device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
+                                  uint32_t tmem_base)
+{
+    const int warp = threadIdx.x / 32;
+    const uint32_t lane = ptx::lane_id();
+    const int q = warp & 3;
+    const int half = (warp - kEpiWarp0) / 4;
+    const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
+    const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
+    const uint32_t swz = (lane >> 1) & 3u;
+    for (int local = 0;; ++local) {
+        int t;
+        if (!__all_sync(0xffffffffu, kth_tile<PAIR, DYN>(p, s, sc, local, t))) break;
+        // the ring entry is read: the scheduler may reuse it kRing tiles on
+        if (DYN && lane == 0) ptx::red_add_release_cta_smem(s.epi_started, 1);
+        const int arow = sc.a_row(p, t);
+        const int nb = sc.col_block(p, t);
+        const uint32_t acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
+        if (!__all_sync(0xffffffffu, arrived)) break;
+        ptx::tc_fence_after();
+        if (p.stats && lane == 0) {
+            const long long idx = static_cast<long long>(p.trace_tiles) * (p.k_slices + 1) + t;
+            if (idx < p.ctrl.trace_cap)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
+#pragma unroll 1
+        for (int bx = 0; bx < kTileN / 2 / kEpiBoxCols; ++bx) {
+            // the previous store from this buffer has finished reading it
+            if (lane == 0) ptx::bulk_wait_read<0>();
+            __syncwarp();
+            {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + bx * kEpiBoxCols, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t chunk = static_cast<uint32_t>(v) ^ swz;
+                    ptx::st_shared_v4(row_addr + chunk * 16,
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                }
+            }
+            if (bx == kTileN / 2 / kEpiBoxCols - 1) {
+                // this warp's reads of the accumulator are done: one arrival per warp
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (PAIR == 1) ptx::mbar_arrive(&s.tempty[acc]);
+                    else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
+                }
+            }
+            // the box's generic-proxy writes are visible to the tensor store
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                  arow + q * 32);
+                ptx::bulk_commit();
+            }
+        }
+        if (p.mode == kModeReduceScatter) {
+            // Publish the partial tile ("cross-GPU sync protocols on PCIe",
+            // section 3): once this warp's stores have written global memory,
+            // it arrives on the tile's counter with its share of the
+            // 64-unit quota; the arrival that completes the count is elected
+            // and release-stores the sequence into the tile's slot.
+            if (lane == 0) {
+                ptx::bulk_wait<0>();
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
+            static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
+            if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
+            __syncwarp();
+        }
+        if (p.stats && lane == 0) {
+            const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
+            if (idx < p.ctrl.trace_cap)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
+    }
+    // every store has written global memory before the CTA retires
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+}
+
+}  // namespace dyn
+
 template <int PAIR>
 __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 {
@@ -602,10 +911,18 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     ptx::grid_dep_wait();
     const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
 
-    if (warp == 0) consumer_tma<PAIR>(p, s, sc);
-    else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
-    else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
-    else if (warp == kGateWarp && (p.gated || sc.dyn)) consumer_gate<PAIR>(p, s, sc);
+    if (PAIR == 1 && sc.dyn) {
+        // role switch: single-CTA tiles from the ticket counter
+        if (warp == 0) dyn::consumer_tma<PAIR, true>(p, s, sc);
+        else if (warp == 1) dyn::consumer_mma<PAIR, true>(p, s, sc, tmem_base);
+        else if (warp < kEpiWarp0 + kEpiWarps) dyn::consumer_epilogue<PAIR, true>(p, s, sc, tmem_base);
+        else if (warp == kGateWarp) dyn::consumer_gate<PAIR, true>(p, s, sc);
+    } else {
+        if (warp == 0) consumer_tma<PAIR>(p, s, sc);
+        else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
+        else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
+        else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
+    }
     __syncwarp();
 
     // teardown: every role of both CTAs has finished before TMEM is freed

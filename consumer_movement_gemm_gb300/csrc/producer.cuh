@@ -325,7 +325,7 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
 // fp32, ascending s, and stores the bf16 result, four rows at a time.  Lane l
 // owns the 16-byte column group l of each row (32 groups = 256 columns).
 // Shards are read four at a time, so each lane has 16 loads in flight.
-__device__ inline void rs_reduce(const FusedParams& p)
+static __device__ __noinline__ void rs_reduce(const FusedParams& p)
 {
     constexpr int kItemRows = 16;
     constexpr int kRows = 4;
