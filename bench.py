@@ -358,15 +358,18 @@ def e2e_tp(h, cfg, W, gathered, out, steps: int, stream):
             "h2d_bytes_per_step": X_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
 
 
-def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int):
-    """Dispatch + grouped GEMM: algorithmic TFLOP/s (real rows only)."""
+def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int, align: int = 128):
+    """Dispatch + grouped GEMM: algorithmic TFLOP/s (real rows only).  `align`
+    = expert segment alignment (128, the pages' row block; 256 lets CTA pairs
+    take 256-row tiles inside one expert)."""
     import numpy as np
     import torch
     import workloads
     from consumer_movement_gemm_gb300 import tovl
     x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
-    rows = tovl.dispatch_rows(cfg.T, cfg.k, cfg.E)
+    rows = tovl.dispatch_rows_aligned(cfg.T, cfg.k, cfg.E, align)
     with tovl.Handle(0, max_rows=rows, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=k_slices) as h:
+        h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
         if producers:
             h.set_option(tovl.OPT_PRODUCERS, producers)
         topk = torch.from_numpy(topk_np).to(dev)
@@ -382,7 +385,8 @@ def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int):
         counts = np.bincount(topk_np.reshape(-1), minlength=cfg.E)
         m_pad = int(offs[-1].item())
         flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.N
-        res = {"workload": cfg.name, "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+        res = {"workload": cfg.name, "segment_alignment": align, "pair_tiles": bool(h.get_option(tovl.OPT_PAIRS)) and align == 256,
+               "producer_ctas": h.get_option(tovl.OPT_PRODUCERS), "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
                "algorithmic_GFLOP": flops / 1e9, "padded_rows": m_pad, "max_expert_rows": int(counts.max()),
                "min_expert_rows": int(counts.min()), "rounds": rounds, "l2": "flushed before every round"}
         res["combine"] = combine_bench(h, cfg, out, timer, rounds, dev)
@@ -548,6 +552,10 @@ def run_tovl(args):
                                                    dev, args.producers, args.k_slices)
         extra["dispatch_zipf"] = dispatch_bench(workloads.SKEWED, 20 if not args.full else workloads.SKEWED.rounds * 10,
                                                 dev, args.producers, args.k_slices)
+        extra["dispatch_uniform_pairs"] = dispatch_bench(workloads.DISPATCH, 30 if not args.full else workloads.DISPATCH.rounds * 10,
+                                                         dev, args.producers, args.k_slices, align=256)
+        extra["dispatch_zipf_pairs"] = dispatch_bench(workloads.SKEWED, 20 if not args.full else workloads.SKEWED.rounds * 10,
+                                                      dev, args.producers, args.k_slices, align=256)
         extra["gemm_reduce_scatter"] = rs_bench(workloads.TP, 30 if not args.full else 200, dev)
         sizes = list(workloads.COPY.row_sizes)
         extra["gated_copy"] = copy_sweep(1000 if args.full else 20, dev, sizes)

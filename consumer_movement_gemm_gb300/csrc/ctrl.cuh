@@ -173,6 +173,7 @@ struct PlanParams {
     Plan plan;
     int* status;
     int* work;            // ticket counter of the fused kernel that follows (zeroed here)
+    int align;            // expert segments start at multiples of this many rows (128 or 256)
 };
 
 struct CopyParams {

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         int run = 0;
         s_off[0] = 0;
         for (int e = 0; e < p.E; ++e) {
-            run += (s_cnt[e] + kBlockRows - 1) / kBlockRows * kBlockRows;
+            run += (s_cnt[e] + p.align - 1) / p.align * p.align;
             s_off[e + 1] = run;
         }
         if (run > p.row_cap || run / kBlockRows > p.block_cap) s_bad = 1;
@@ -131,12 +131,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         p.plan.meta[2] = s_zero;
         p.plan.meta[3] = 0;
     }
-    // block tables and padding rows of each expert segment
+    // block tables and padding rows of each expert segment: a block holds
+    // min(128, rows of the segment left) real rows, the rest is padding (with
+    // 256-row segments the last two blocks may both be padded)
     for (int e = tid; e < p.E; e += kPlanThreads) {
         const int b0 = s_off[e] / kBlockRows, b1 = s_off[e + 1] / kBlockRows;
         for (int b = b0; b < b1; ++b) {
             p.plan.blk_expert[b] = e;
-            p.plan.pad[b] = (b == b1 - 1) ? (s_off[e + 1] - s_off[e] - s_cnt[e]) : 0;
+            const int real = min(max(s_cnt[e] - (b - b0) * kBlockRows, 0), kBlockRows);
+            p.plan.pad[b] = kBlockRows - real;
         }
         for (int r = s_off[e] + s_cnt[e]; r < s_off[e + 1]; ++r) p.plan.src_of_dst[r] = -1;
     }

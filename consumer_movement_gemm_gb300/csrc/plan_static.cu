@@ -105,6 +105,7 @@ TOVL_API int tovl_dispatch_plan_noalloc(const int* topk_idx, int T, int k, int E
     pp.plan.blk_expert = base + kOffBlk;
     pp.plan.meta = base + kOffMeta;
     pp.status = base + kOffStatus;
+    pp.align = kBlockRows;
     // The array keeps the previous call's contents; the routing-error flag in
     // meta must start at zero (every other piece is overwritten before use).
     if (cudaMemsetAsync(base + kOffMeta, 0, 4 * sizeof(int), s) != cudaSuccess) return TOVL_ERR_CUDA;

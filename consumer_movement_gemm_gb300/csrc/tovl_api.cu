@@ -42,6 +42,7 @@ struct tovl_ctx {
     bool coop_pairs = true;  // cooperative launch accepted together with clusters
     bool coop_enabled = true;  // fused launches ask for the co-residency guarantee
     int producer_mode = 0;     // fused producers: 0 vector copies, 1 staged bulk loads
+    int dispatch_align = kBlockRows;  // expert segment alignment: 128, or 256 for CTA-pair tiles
     bool pdl = true;           // programmatic dependent launch between this library's kernels
     bool role_switch = true;   // reduce-scatter consumers join the reduction after their tiles
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
@@ -111,11 +112,15 @@ TOVL_API const char* tovl_last_error(tovl_handle h)
     return h ? h->last_error : "";
 }
 
+TOVL_API long long tovl_dispatch_rows_aligned(int T, int k, int E, int align)
+{
+    if (T < 0 || k < 0 || E < 0 || (align != kBlockRows && align != 2 * kBlockRows)) return 0;
+    return ceil_div(static_cast<long long>(T) * k + static_cast<long long>(E) * (align - 1), align) * align;
+}
+
 TOVL_API long long tovl_dispatch_rows(int T, int k, int E)
 {
-    if (T < 0 || k < 0 || E < 0) return 0;
-    return ceil_div(static_cast<long long>(T) * k + static_cast<long long>(E) * (kBlockRows - 1), kBlockRows) *
-           kBlockRows;
+    return tovl_dispatch_rows_aligned(T, k, E, kBlockRows);
 }
 
 static void free_all(tovl_ctx* h)
@@ -552,8 +557,11 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     if (N < kTileN || N % kTileN) return TOVL_ERR_UNSUPPORTED;
     const long long pairs = static_cast<long long>(T) * k;
     if (pairs > h->cfg.max_pairs) return TOVL_ERR_INVALID;
-    const long long rows = tovl_dispatch_rows(T, k, E);
+    const int align = h->dispatch_align;
+    const long long rows = tovl_dispatch_rows_aligned(T, k, E, align);
     if (rows > h->cfg.max_rows) return TOVL_ERR_INVALID;
+    // 256-row segments let a CTA pair take two row blocks of one expert
+    const int pair = (align == 2 * kBlockRows && h->pair_mode && h->max_pairs > 0) ? 2 : 1;
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -571,6 +579,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     pp.plan = h->plan;
     pp.status = h->ctrl.status;
     pp.work = h->ctrl.work;
+    pp.align = align;
     cudaError_t e = launch_plan(pp, s, h->pdl && h->pdl_ok);
     if (e != cudaSuccess && h->pdl && h->pdl_ok) {
         cudaGetLastError();
@@ -589,16 +598,18 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.n_nb = N / kTileN;
     p.row_bytes = H * 2;
     int P, C;
+    // role switch (single-CTA tiles): consumer tiles come from the ticket
+    // counter (zeroed by the plan kernel) and producer CTAs take tiles once
+    // their copies are done
+    const bool dyn = h->role_switch && pair == 1;
     split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
-               2.0 * pairs * static_cast<double>(N) * H, 1, h->role_switch);
+               2.0 * pairs * static_cast<double>(N) * H, pair, dyn);
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 1;
-    // role switch: consumer tiles come from the ticket counter (zeroed by the
-    // plan kernel) and producer CTAs take tiles once their copies are done
-    p.dyn = h->role_switch ? 1 : 0;
-    p.join = h->role_switch ? 1 : 0;
-    call_geometry(h, p, C, 1);
+    p.dyn = dyn ? 1 : 0;
+    p.join = dyn ? 1 : 0;
+    call_geometry(h, p, C, pair);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;
     p.pad = h->plan.pad;
@@ -618,9 +629,9 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
         return rc;
     p.seq = static_cast<int>(h->seq + 1);
     p.gate_seq = p.seq + h->fault_gate_offset;
-    p.trace_tiles = static_cast<int>(rows / kTileM * p.n_nb);
+    p.trace_tiles = static_cast<int>(rows / kTileM / pair * p.n_nb);
     if ((rc = reset_stats(h, s, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
-    e = launch(h, p, s, true, 1);
+    e = launch(h, p, s, true, pair);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
     h->seq += 1;
     h->last_stream = s;
@@ -995,6 +1006,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != 0 && value != 1) return TOVL_ERR_INVALID;
         h->role_switch = value != 0;
         return TOVL_OK;
+    case 17:
+        if (value != kBlockRows && value != 2 * kBlockRows) return TOVL_ERR_INVALID;
+        h->dispatch_align = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -1020,6 +1035,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 14: *value = h->producer_mode; return TOVL_OK;
     case 15: *value = (h->pdl && h->pdl_ok) ? 1 : 0; return TOVL_OK;
     case 16: *value = h->role_switch ? 1 : 0; return TOVL_OK;
+    case 17: *value = h->dispatch_align; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

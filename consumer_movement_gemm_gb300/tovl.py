@@ -40,6 +40,7 @@ OPT_COOPERATIVE = 13
 OPT_PRODUCER_MODE = 14
 OPT_PDL = 15
 OPT_ROLE_SWITCH = 16
+OPT_DISPATCH_ALIGN = 17
 
 
 class TovlError(RuntimeError):
@@ -80,6 +81,7 @@ SIGNATURES = {
     "tovl_destroy": ([_P], _I),
     "tovl_gather_gemm": ([_P, ctypes.POINTER(_P), _I, _I, _I, _P, _I, _P, _P, _P], _I),
     "tovl_dispatch_rows": ([_I, _I, _I], _LL),
+    "tovl_dispatch_rows_aligned": ([_I, _I, _I, _I], _LL),
     "tovl_dispatch_grouped_gemm": ([_P, _P, _I, _I, _P, _I, _I, _P, _I, _P, _P, _P, _P], _I),
     "tovl_combine": ([_P, _P, _I, _P, _P, _P, _P], _I),
     "tovl_gemm_reduce_scatter": ([_P, _P, _I, _I, _I, _P, _I, _P, _P, _P], _I),
@@ -158,6 +160,11 @@ def default_config(device: int = 0) -> tovl_config:
 
 def dispatch_rows(T: int, k: int, E: int) -> int:
     return load().tovl_dispatch_rows(T, k, E)
+
+
+def dispatch_rows_aligned(T: int, k: int, E: int, align: int) -> int:
+    """Rows a dispatch buffer needs with expert segments aligned to ``align``."""
+    return int(load().tovl_dispatch_rows_aligned(T, k, E, align))
 
 
 def dispatch_plan_noalloc(topk, E: int, expert_offsets, dst_rows, stream=None) -> None:
@@ -272,7 +279,7 @@ class Handle:
 
     def read_plan(self, T: int, k: int, E: int):
         import numpy as np
-        rows = dispatch_rows(T, k, E)
+        rows = dispatch_rows_aligned(T, k, E, self.get_option(OPT_DISPATCH_ALIGN))
         counts = np.zeros(E, np.int32)
         dst = np.zeros(T * k, np.int32)
         src = np.zeros(max(rows, 1), np.int32)

@@ -113,6 +113,11 @@ int tovl_gather_gemm(tovl_handle h, const void* const* shards, int num_shards, i
 /* Rows a dispatch buffer needs: T*k + E*127 rounded up to a multiple of 128. */
 long long tovl_dispatch_rows(int T, int k, int E);
 
+/* The same bound for expert segments aligned to `align` rows (128, or 256 with
+ * option 17): T*k + E*(align-1) rounded up to a multiple of align; 0 for any
+ * other align. */
+long long tovl_dispatch_rows_aligned(int T, int k, int E, int align);
+
 /* Dispatch scatter of top-k routed tokens into padded per-expert segments,
  * followed by a grouped GEMM per expert (notify-stage counting of the DeepEP
  * FIFO-pipeline page; row-block counters with padding seeds of section 5).
@@ -290,6 +295,12 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * automatic split then gives the copy twice its balance share); in
  * tovl_gemm_reduce_scatter consumer CTAs that have finished their partial
  * tiles take reduction items beside the producer CTAs,
+ * 17 = expert segment alignment of tovl_dispatch_grouped_gemm in rows: 128
+ * (the default: segments padded to the 128-row block, the layout the oracle
+ * defines) or 256 (segments padded to two blocks, so CTA pairs compute
+ * 256-row tiles inside one expert; the padded rows are zero and their
+ * block counters are seeded like any padding; buffers then need
+ * tovl_dispatch_rows_aligned(T, k, E, 256) rows),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

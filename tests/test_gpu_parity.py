@@ -219,6 +219,40 @@ def test_dispatch_grouped_gemm_small(routing, k_slices, mode, switch):
             _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
 
 
+@pytest.mark.parametrize("routing", list(ROUTINGS))
+def test_dispatch_pair_tiles_on_256_row_segments(routing):
+    # option 17: segments aligned to 256 rows, CTA-pair tiles; the layout is
+    # the oracle's plan with 256-row blocks, the counters stay per 128 rows
+    H, N = 192, 512
+    with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_DISPATCH_ALIGN, 256)
+        for r in range(1, 4):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(3, r))
+            T, k = topk_np.shape
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 900 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 950 + r, DEV)
+            rows = tovl.dispatch_rows_aligned(T, k, E, 256)
+            dispatched = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device=DEV)
+            offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+            out = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+            h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
+            assert h.sync_status() == 0
+            p = oracle.dispatch_plan(topk_np, E, block_rows=256)
+            counts, dst, src, pad, blk, m_pad = h.read_plan(T, k, E)
+            assert m_pad == p.m_pad and m_pad % 256 == 0
+            assert np.array_equal(offs.cpu().numpy(), p.off)
+            assert np.array_equal(dst, p.dst)
+            assert np.array_equal(src, p.src)
+            # per 128-row block: padding = rows without a source, expert = segment
+            real = (p.src >= 0).reshape(-1, 128).sum(axis=1)
+            assert np.array_equal(pad, 128 - real)
+            assert np.array_equal(blk, np.searchsorted(p.off, np.arange(0, m_pad, 128), side="right") - 1)
+            D = oracle.dispatch(bits(x), p.dst, k, p.m_pad)
+            assert np.array_equal(bits(dispatched[:m_pad]), D), "dispatched buffer"
+            assert_close(out[:m_pad], oracle.grouped_matmul_f32(D, bits(W), p.off), "grouped GEMM, pair tiles")
+            _check_ctrl(h, r)
+
+
 def test_dispatch_bad_expert_id_is_a_noop_round():
     H, N, E = 64, 256, 3
     with _handle() as h:
