@@ -139,6 +139,11 @@ struct PermRowJob {
 
 // Waiters: warp w watches chunks [w*per, (w+1)*per); lane i of the warp owns
 // chunks c = base + i + 32*j.  A lane re-polls only chunks it has not seen.
+// Eight slots per lane are read per pass with relaxed (strong) loads, so the
+// eight reads are in flight together; a lane that sees a slot reach the
+// round's sequence takes an acquire fence before it stamps the observation
+// -- a strong read followed by the fence is an acquire of that slot (eight
+// back-to-back acquire loads would each wait for the one before).
 __device__ void copy_waiter(const CopyParams& p, int ww, int n_ww)
 {
     const uint32_t lane = ptx::lane_id();
@@ -160,9 +165,13 @@ __device__ void copy_waiter(const CopyParams& p, int ww, int n_ww)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int c = c0 + static_cast<int>(lane) + 32 * (j + u);
-                val[u] = (j + u < cpl && c < c1 && !((seen_bits >> (j + u)) & 1ull)) ? ptx::ld_acquire_gpu(p.ctrl.slot + c * p.ctrl.n_slices)
+                val[u] = (j + u < cpl && c < c1 && !((seen_bits >> (j + u)) & 1ull)) ? ptx::ld_relaxed_gpu(p.ctrl.slot + c * p.ctrl.n_slices)
                                                                                         : -2147483647;
             }
+            bool any = false;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) any |= val[u] >= p.seq;
+            if (any) ptx::fence_acq_rel_gpu();
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 if (val[u] >= p.seq) {
