@@ -55,6 +55,25 @@ def test_dispatch_rows_closed_form(lib):
         assert tovl.dispatch_rows(T, k, E) == want
 
 
+def test_dispatch_rows_aligned_closed_form(lib):
+    for T, k, E in [(4096, 2, 8), (8192, 4, 32), (1, 1, 1), (0, 2, 3)]:
+        assert tovl.dispatch_rows_aligned(T, k, E, 128) == tovl.dispatch_rows(T, k, E)
+        want = -(-(T * k + E * 255) // 256) * 256
+        assert tovl.dispatch_rows_aligned(T, k, E, 256) == want
+    assert tovl.dispatch_rows_aligned(10, 2, 3, 192) == 0       # only 128 and 256
+    assert tovl.dispatch_rows_aligned(-1, 2, 3, 128) == 0
+
+
+def test_new_entry_points_reject_null_handles(lib):
+    L = tovl.load()
+    assert L.tovl_combine(None, None, 0, None, None, None, None) == tovl.TOVL_ERR_INVALID
+    assert L.tovl_gemm_reduce_scatter(None, None, 0, 0, 0, None, 0, None, None, None) == tovl.TOVL_ERR_INVALID
+    v = ctypes.c_longlong()
+    for opt in (14, 15, 16, 17):
+        assert L.tovl_set_option(None, opt, 0) == tovl.TOVL_ERR_INVALID
+        assert L.tovl_get_option(None, opt, ctypes.byref(v)) == tovl.TOVL_ERR_INVALID
+
+
 def test_host_argument_errors(lib):
     L = tovl.load()
     assert L.tovl_create(None, None) == tovl.TOVL_ERR_INVALID

@@ -311,6 +311,27 @@ def test_combine_after_dispatch(routing, mode, pdl):
             _check_ctrl(h, R)
 
 
+def test_combine_after_pair_tile_dispatch():
+    # the 256-row segment layout changes where expert rows live, not combine
+    H, N, T, k, E = 128, 256, 300, 2, 5
+    with _handle() as h:
+        h.set_option(tovl.OPT_DISPATCH_ALIGN, 256)
+        topk_np = workloads.uniform_topk(T, k, E, 31)
+        x = workloads.bf16_normal((T, H), 1.0, 32, DEV)
+        W = workloads.bf16_normal((E, H, 256), 1.0, 33, DEV)
+        rows = tovl.dispatch_rows_aligned(T, k, E, 256)
+        dispatched = torch.zeros(rows, H, dtype=torch.bfloat16, device=DEV)
+        offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+        out = torch.empty(rows, 256, dtype=torch.bfloat16, device=DEV)
+        h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
+        y, w_np, staging, combined = _combine_round(h, rows, N, T, k, 34)
+        assert h.sync_status() == 0
+        S, C = oracle.combine(bits(y), oracle.dispatch_plan(topk_np, E, block_rows=256).dst, w_np)
+        assert np.array_equal(bits(staging[:T * k]), S)
+        assert np.array_equal(bits(combined[:T]), C)
+        _check_ctrl(h, 2)
+
+
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (21, 3, 5), (64, 1, 2), (100, 8, 16)])
 def test_combine_shapes(T, k, E):
     # one token; tokens straddling 64-row chunks (k=3); exactly one chunk;
