@@ -105,10 +105,12 @@ def test_tiny_gather_gemm_three_rounds(k_slices, pairs, mode):
 
 
 # item shapes: (3,100,192) 32-row items; (1,64,64) 64-row items; (2,70,8192,KS=1)
-# single-row items wider than one 8 KB pass
+# single-row items wider than one 8 KB pass; (3,150,1024) and (2,300,2048,KS=2)
+# 4-row items with 8 lanes per row
 @pytest.mark.parametrize("S,R,K,N,P,KS", [(3, 100, 192, 256, 4, 2), (1, 64, 64, 512, 1, 4), (5, 77, 128, 256, 32, 1),
                                           (2, 200, 320, 256, 8, 4), (7, 33, 448, 512, 3, 8),
-                                          (2, 70, 8192, 256, 4, 1)])
+                                          (2, 70, 8192, 256, 4, 1), (3, 150, 1024, 256, 4, 1),
+                                          (2, 300, 2048, 512, 6, 2)])
 @pytest.mark.parametrize("pairs", [1, 0])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_gather_gemm_ragged(S, R, K, N, P, KS, pairs, mode):
