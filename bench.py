@@ -331,31 +331,51 @@ def acceptance(h, timer, cfg, X, W, gathered, out, n: int, producers: int):
 
 
 def e2e_tp(h, cfg, W, gathered, out, steps: int, stream):
-    """Host shards -> device, fused call, device -> host output, per step."""
+    """Host shards -> device, fused call, device -> host output, every step.
+    Pipelined like a serving loop: two buffer sets and three streams, so the
+    upload of step i+1 and the download of step i-1 overlap step i's fused
+    call; every step still moves its whole input up and its whole output
+    back.  Time = first upload start to last download end, per step."""
     import torch
     import workloads
     X_host = workloads.gather_inputs(cfg, 0, "cpu")[0].pin_memory()
-    out_host = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16).pin_memory()
-    X_dev = torch.empty_like(X_host, device="cuda")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    X_dev = [torch.empty_like(X_host, device="cuda") for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
+    gath = [gathered, torch.empty_like(gathered)]
+    out_host = [torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # upload of buffer set b done
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # fused call on set b done
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # download of set b done
 
-    def step():
-        X_dev.copy_(X_host, non_blocking=True)
-        h.gather_gemm(X_dev, W, gathered, out, stream=stream)
-        out_host.copy_(out, non_blocking=True)
+    def step(i):
+        b = i % 2
+        s_in.wait_event(ev_done[b])                     # set b's last fused call has read X_dev[b]
+        with torch.cuda.stream(s_in):
+            X_dev[b].copy_(X_host, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])                    # set b's last output has been read back
+        h.gather_gemm(X_dev[b], W, gath[b], outs[b], stream=stream)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            out_host[b].copy_(outs[b], non_blocking=True)
+        ev_out[b].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        stream.synchronize()
-        ev[0].record(stream)
-        for _ in range(steps):
-            step()
-        ev[1].record(stream)
-    stream.synchronize()
-    ms = ev[0].elapsed_time(ev[1]) / steps
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        step(i)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
     return {"value": cfg.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": X_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
+            "h2d_bytes_per_step": X_host.numel() * 2, "d2h_bytes_per_step": out_host[0].numel() * 2,
+            "pipelined": "upload of step i+1 and download of step i-1 overlap step i (two buffer sets, three streams)"}
 
 
 def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int, align: int = 128):
