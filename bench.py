@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", choices=["fused", "gemm", "copy", "dispatch", "combine", "rs"], default=None,
                     help="run only W + K calls of one kernel on a small case (for ncu captures) and exit")
+    ap.add_argument("--dispatch-align", type=int, default=128, choices=[128, 256],
+                    help="expert segment alignment of --profile dispatch/combine (256: CTA-pair tiles)")
     ap.add_argument("--no-coop", action="store_true",
                     help="launch fused kernels without the cooperative attribute (profiler replay)")
     return ap.parse_args(argv)
@@ -666,8 +668,9 @@ def run_profile(args):
     else:
         cfg = workloads.DISPATCH
         x, topk_np, W = workloads.dispatch_inputs(cfg, 0, dev)
-        rows = tovl.dispatch_rows(cfg.T, cfg.k, cfg.E)
+        rows = tovl.dispatch_rows_aligned(cfg.T, cfg.k, cfg.E, args.dispatch_align)
         with tovl.Handle(0, max_rows=rows, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=args.k_slices) as h:
+            h.set_option(tovl.OPT_DISPATCH_ALIGN, args.dispatch_align)
             if args.no_coop:
                 h.set_option(tovl.OPT_COOPERATIVE, 0)
             topk = torch.from_numpy(topk_np).to(dev)
