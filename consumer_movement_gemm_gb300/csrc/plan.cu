@@ -63,11 +63,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const PlanPara
     if (i < p.n_pairs) p.plan.local_rank[i] = (e >= 0) ? wcnt[warp * p.E + e] + rank_in_warp : 0;
 }
 
+// Expert of padded row r: the last e with off[e] <= r (empty experts share
+// their start with the next one).  off[E] is past every row.
+__device__ __forceinline__ int expert_of_row(const int* s_off, int E, int r)
+{
+    int lo = 0, hi = E;             // invariant: s_off[lo] <= r < s_off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Segment bases of the finalize kernel live in shared memory when they fit
+// (the destination step then needs one round of global loads, not two).
+constexpr int kSegSmemInts = 10 * 1024;   // with E <= 512 the kernel stays under 48 KB
+
+// One CTA.  Every step issues its global loads together before it uses them
+// (a single thread walking dependent loads would pay one L2 round trip per
+// element), and the table writes of the last step need no barrier between
+// them.
 __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanParams p)
 {
     extern __shared__ int sm[];
     int* s_off = sm;                // [E+1]
     int* s_cnt = sm + p.E + 1;      // [E]
+    int* s_seg = sm + 2 * p.E + 1;  // [n_seg][E] segment bases, when they fit
+    const bool seg_in_smem = p.n_seg * p.E <= kSegSmemInts;
+    int* seg_base = seg_in_smem ? s_seg : p.plan.seg_count;
     __shared__ int s_zero;
     __shared__ int s_bad;
     // the counting grid (launched just before, programmatically) has finished
@@ -75,18 +99,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
     ptx::grid_dep_launch();         // the fused kernel may start its launch and prologue
     const int tid = threadIdx.x;
     if (tid == 0 && p.work) *p.work = 0;   // the fused kernel's tile tickets start at 0
-    const int* meta_in = p.plan.meta;
     if (tid == 0) {
         s_zero = p.force_zero;
-        s_bad = meta_in[3];
+        s_bad = p.plan.meta[3];
     }
-    // per-expert prefix over segments (becomes each segment's base rank)
+    // per-expert prefix over segments (each segment's base rank), segments
+    // read kPrefixBatch at a time; the previous layout is read alongside
+    constexpr int kPrefixBatch = 8;
+    int prev = 0;
+    if (tid <= p.E) prev = p.plan.prev_off[tid];
     for (int e = tid; e < p.E; e += kPlanThreads) {
         int run = 0;
-        for (int s = 0; s < p.n_seg; ++s) {
-            const int v = p.plan.seg_count[s * p.E + e];
-            p.plan.seg_count[s * p.E + e] = run;
-            run += v;
+        for (int s0 = 0; s0 < p.n_seg; s0 += kPrefixBatch) {
+            int v[kPrefixBatch];
+#pragma unroll
+            for (int j = 0; j < kPrefixBatch; ++j)
+                v[j] = (s0 + j < p.n_seg) ? p.plan.seg_count[(s0 + j) * p.E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kPrefixBatch; ++j) {
+                if (s0 + j < p.n_seg) seg_base[(s0 + j) * p.E + e] = run;
+                run += v[j];
+            }
         }
         s_cnt[e] = run;
         p.plan.counts[e] = run;
@@ -102,8 +135,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         if (run > p.row_cap || run / kBlockRows > p.block_cap) s_bad = 1;
     }
     __syncthreads();
-    const bool bad = s_bad != 0;
-    if (bad) {
+    if (tid <= p.E && prev != s_off[tid]) s_zero = 1;     // benign race: every writer stores 1
+    for (int e = tid + kPlanThreads; e <= p.E; e += kPlanThreads)
+        if (p.plan.prev_off[e] != s_off[e]) s_zero = 1;
+    __syncthreads();
+    if (s_bad != 0) {
         if (tid == 0) {
             ptx::atom_cas_relaxed_gpu(p.status, kOk, kErrInvalid);
             p.plan.meta[0] = 0;
@@ -114,11 +150,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         for (int e = tid; e <= p.E; e += kPlanThreads) p.expert_offsets[e] = 0;
         return;
     }
-    // layout change decides whether padding rows must be re-zeroed
-    for (int e = tid; e <= p.E; e += kPlanThreads) {
-        if (p.plan.prev_off[e] != s_off[e]) s_zero = 1;   // benign race: every writer stores 1
-    }
-    __syncthreads();
     for (int e = tid; e <= p.E; e += kPlanThreads) {
         p.plan.off[e] = s_off[e];
         p.plan.prev_off[e] = s_off[e];
@@ -131,25 +162,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         p.plan.meta[2] = s_zero;
         p.plan.meta[3] = 0;
     }
-    // block tables and padding rows of each expert segment: a block holds
-    // min(128, rows of the segment left) real rows, the rest is padding (with
-    // 256-row segments the last two blocks may both be padded)
-    for (int e = tid; e < p.E; e += kPlanThreads) {
-        const int b0 = s_off[e] / kBlockRows, b1 = s_off[e + 1] / kBlockRows;
-        for (int b = b0; b < b1; ++b) {
-            p.plan.blk_expert[b] = e;
-            const int real = min(max(s_cnt[e] - (b - b0) * kBlockRows, 0), kBlockRows);
-            p.plan.pad[b] = kBlockRows - real;
+    // destination row of every pair and the inverse map, kDstBatch pairs per
+    // thread at a time: the routing and in-segment ranks are loaded together
+    constexpr int kDstBatch = 8;
+    for (int i0 = 0; i0 < p.n_pairs; i0 += kPlanThreads * kDstBatch) {
+        int e[kDstBatch], lr[kDstBatch];
+#pragma unroll
+        for (int j = 0; j < kDstBatch; ++j) {
+            const int i = i0 + j * kPlanThreads + tid;
+            e[j] = i < p.n_pairs ? p.topk[i] : 0;
+            lr[j] = i < p.n_pairs ? p.plan.local_rank[i] : 0;
         }
-        for (int r = s_off[e] + s_cnt[e]; r < s_off[e + 1]; ++r) p.plan.src_of_dst[r] = -1;
+#pragma unroll
+        for (int j = 0; j < kDstBatch; ++j) {
+            const int i = i0 + j * kPlanThreads + tid;
+            if (i < p.n_pairs) {
+                const int d = s_off[e[j]] + seg_base[(i / kPlanThreads) * p.E + e[j]] + lr[j];
+                p.plan.dst[i] = d;
+                p.plan.src_of_dst[d] = i / p.k;
+            }
+        }
     }
-    // destination row of every pair and the inverse map
-    for (int i = tid; i < p.n_pairs; i += kPlanThreads) {
-        const int e = p.topk[i];
-        const int seg = i / kPlanThreads;
-        const int d = s_off[e] + p.plan.seg_count[seg * p.E + e] + p.plan.local_rank[i];
-        p.plan.dst[i] = d;
-        p.plan.src_of_dst[d] = i / p.k;
+    // block tables: a block holds min(128, rows of its segment left) real
+    // rows, the rest is padding (with 256-row segments the last two blocks
+    // of a segment may both be padded)
+    for (int b = tid; b < m_pad / kBlockRows; b += kPlanThreads) {
+        const int e = expert_of_row(s_off, p.E, b * kBlockRows);
+        p.plan.blk_expert[b] = e;
+        const int real = min(max(s_cnt[e] - (b * kBlockRows - s_off[e]), 0), kBlockRows);
+        p.plan.pad[b] = kBlockRows - real;
+    }
+    // padding rows (fewer than `align` per expert) have no source token
+    for (int x = tid; x < p.E * p.align; x += kPlanThreads) {
+        const int e = x / p.align;
+        const int r = s_off[e] + s_cnt[e] + x % p.align;
+        if (r < s_off[e + 1]) p.plan.src_of_dst[r] = -1;
     }
 }
 
@@ -162,7 +209,8 @@ namespace tovl {
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream, bool pdl)
 {
     const size_t sm_count = static_cast<size_t>(kPlanWarps) * p.E * sizeof(int);
-    const size_t sm_fin = static_cast<size_t>(2 * p.E + 1) * sizeof(int);
+    const size_t seg = static_cast<size_t>(p.n_seg) * p.E;
+    const size_t sm_fin = (2 * static_cast<size_t>(p.E) + 1 + (seg <= kSegSmemInts ? seg : 0)) * sizeof(int);
     if (p.n_seg > 0) {
         plan_count_kernel<<<p.n_seg, kPlanThreads, sm_count, stream>>>(p);
         const cudaError_t e = cudaGetLastError();
