@@ -57,7 +57,7 @@ struct ConsumerSmem {
     int* ring;           // dynamic schedule: kRing tile indices handed to the other roles (-1 = no more)
     int* ring_head;      // entries published
     int* epi_started;    // epilogue warps' tile starts (kEpiWarps per tile): ring entries that are free
-    int* tma_done;       // tiles whose loads the TMA warp has all issued
+    int* tma_done;       // k-blocks whose loads the TMA warp has issued (dynamic schedule)
 };
 
 constexpr int kRing = 8;
@@ -93,7 +93,7 @@ template <int PAIR>
 struct Schedule {
     int unit, n_units, n_tiles;
     uint32_t rank;
-    bool dyn;            // tiles come from the ticket counter through the ring (single CTAs only)
+    bool dyn;            // tiles come from the ticket counter through the ring
     __device__ int out_tile(const FusedParams& p, int t) const
     {
         return p.mode == kModeReduceScatter ? t / p.n_shards : t;
@@ -120,7 +120,7 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     sc.unit = cid / PAIR;
     sc.n_units = p.n_consumers / PAIR;
     sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb * (p.mode == kModeReduceScatter ? p.n_shards : 1);
-    sc.dyn = PAIR == 1 && p.dyn;
+    sc.dyn = p.dyn != 0;
     return sc;
 }
 
@@ -475,21 +475,30 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     __syncwarp();
 }
 
-// Role switch, dynamic schedule (single-CTA tiles): the same roles as above,
+// Role switch, dynamic schedule (single CTAs or CTA pairs): the same roles as above,
 // with tiles taken from the round's ticket counter through a shared-memory
 // ring instead of a fixed stride.  Kept apart from the fixed-schedule roles so
 // those compile exactly as they are.
 namespace dyn {
+
+// Entries of the ring published so far.  A CTA pair shares one schedule:
+// the pair's first CTA writes both CTAs' rings, so a pair reads its head at
+// cluster scope.
+template <int PAIR>
+__device__ __forceinline__ int ring_published(const ConsumerSmem<PAIR>& s)
+{
+    return PAIR == 2 ? ptx::ld_acquire_cluster_smem(s.ring_head) : ptx::ld_acquire_cta_smem(s.ring_head);
+}
 
 // Dynamic schedule: wait (bounded) until the scheduler has published ring
 // entry k.  Returns false on a pipeline timeout.
 template <int PAIR>
 __device__ __forceinline__ bool ring_wait(const FusedParams& p, const ConsumerSmem<PAIR>& s, int k)
 {
-    if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+    if (ring_published<PAIR>(s) > k) return true;
     const uint64_t start = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (ptx::ld_acquire_cta_smem(s.ring_head) > k) return true;
+        if (ring_published<PAIR>(s) > k) return true;
         if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
             record_error(p.ctrl, kErrTimeout);
             return false;
@@ -514,23 +523,35 @@ __device__ __forceinline__ bool kth_tile(const FusedParams& p, const ConsumerSme
 }
 
 // Dynamic schedule (role switch): the gate warp is also the CTA's scheduler.
-// It takes the next tile from the round's ticket counter when the TMA warp
-// has issued every load of the current one -- the moment the pipeline needs
-// it, so no CTA holds a tile another could start sooner -- publishes it in
+// It takes the next tile from the round's ticket counter once the TMA warp
+// has issued half of the current tile's loads -- early enough that the new
+// tile's gates are passed before the pipeline drains, late enough that no
+// CTA holds a tile another could start sooner -- publishes it in
 // the ring (CTA-scope release) and then waits for that tile's gates.  A ring
 // entry is reused only after the epilogue warps have started its tile.  A
-// ticket past the last tile publishes -1 and ends every role.
+// ticket past the last tile publishes -1 and ends every role.  In a CTA pair
+// the first CTA's gate warp schedules for both: it also waits for the other
+// CTA's epilogue warps before it reuses an entry, writes the tile into both
+// rings and releases both heads at cluster scope; the second CTA's gate
+// warp reads its ring like the other roles.
 template <int PAIR>
 __device__ int sched_next(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc, int k)
 {
     const uint32_t lane = ptx::lane_id();
     int t = -1;
+    if (PAIR == 2 && sc.rank != 0) {
+        if (lane == 0 && ring_wait<PAIR>(p, s, k)) t = s.ring[k % kRing];
+        return __shfl_sync(0xffffffffu, t, 0);
+    }
     if (lane == 0) {
         bool room = true;
         const int need_epi = k >= kRing ? kEpiWarps * (k - kRing + 1) : 0;
+        const uint32_t peer_epi = PAIR == 2 ? ptx::mapa_shared(ptx::smem_u32(s.epi_started), 1) : 0u;
         const uint64_t start = ptx::globaltimer();
-        for (uint32_t i = 1; ptx::ld_acquire_cta_smem(s.tma_done) < k ||
-                             ptx::ld_acquire_cta_smem(s.epi_started) < need_epi; ++i) {
+        const int need_kb = k * p.n_kb - p.n_kb / 2;
+        for (uint32_t i = 1; ptx::ld_acquire_cta_smem(s.tma_done) < need_kb ||
+                             ptx::ld_acquire_cta_smem(s.epi_started) < need_epi ||
+                             (PAIR == 2 && ptx::ld_acquire_cluster_remote(peer_epi) < need_epi); ++i) {
             if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
                 record_error(p.ctrl, kErrTimeout);
                 room = false;
@@ -542,8 +563,15 @@ __device__ int sched_next(const FusedParams& p, const ConsumerSmem<PAIR>& s, con
             t = ptx::atom_add_relaxed_gpu(p.ctrl.work, 1);
             if (t >= sc.n_tiles) t = -1;
         }
-        s.ring[k % kRing] = t;
-        ptx::st_release_cta_smem(s.ring_head, k + 1);
+        if (PAIR == 2) {
+            for (uint32_t r = 0; r < 2; ++r) {
+                ptx::st_cluster_remote(ptx::mapa_shared(ptx::smem_u32(&s.ring[k % kRing]), r), t);
+                ptx::st_release_cluster_remote(ptx::mapa_shared(ptx::smem_u32(s.ring_head), r), k + 1);
+            }
+        } else {
+            s.ring[k % kRing] = t;
+            ptx::st_release_cta_smem(s.ring_head, k + 1);
+        }
     }
     return __shfl_sync(0xffffffffu, t, 0);
 }
@@ -601,7 +629,7 @@ __device__ __forceinline__ int b_resolve(const FusedParams& p, const ConsumerSme
     if constexpr (!DYN) {
         t = sc.unit + b.k * sc.n_units;
     } else {
-        if (ptx::ld_acquire_cta_smem(s.ring_head) <= b.k) {
+        if (ring_published<PAIR>(s) <= b.k) {
             if (!block) return 0;
             if (!ring_wait<PAIR>(p, s, b.k)) return -1;
         }
@@ -739,8 +767,8 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 ++a_count;
                 if (++stage == T::kStages) stage = 0;
             }
+            if constexpr (DYN) ptx::st_release_cta_smem(s.tma_done, k * p.n_kb + kb1);
         }
-        if constexpr (DYN) ptx::st_release_cta_smem(s.tma_done, k + 1);
     }
 }
 
@@ -813,7 +841,10 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         int t;
         if (!__all_sync(0xffffffffu, kth_tile<PAIR, DYN>(p, s, sc, local, t))) break;
         // the ring entry is read: the scheduler may reuse it kRing tiles on
-        if (DYN && lane == 0) ptx::red_add_release_cta_smem(s.epi_started, 1);
+        if (DYN && lane == 0) {
+            if (PAIR == 2) ptx::red_add_release_cluster_smem(s.epi_started, 1);   // the first CTA schedules
+            else ptx::red_add_release_cta_smem(s.epi_started, 1);
+        }
         const int arow = sc.a_row(p, t);
         const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
@@ -940,8 +971,8 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     ptx::grid_dep_wait();
     const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
 
-    if (PAIR == 1 && sc.dyn) {
-        // role switch: single-CTA tiles from the ticket counter
+    if (sc.dyn) {
+        // role switch: tiles from the ticket counter
         if (warp == 0) dyn::consumer_tma<PAIR, true>(p, s, sc);
         else if (warp == 1) dyn::consumer_mma<PAIR, true>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) dyn::consumer_epilogue<PAIR, true>(p, s, sc, tmem_base);

@@ -38,10 +38,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     uint8_t* smem = align1024(smem_raw);
     if (static_cast<int>(blockIdx.x) < p.n_producers) {
         producer(p, smem, blockIdx.x);
-        // role switch: with its copies done, the producer CTA takes GEMM tiles
-        // from the round's ticket counter like any consumer (dispatch rounds,
-        // single-CTA tiles only)
-        if (PAIR == 1 && p.join) consumer<PAIR>(p, smem, -1);
+        // role switch: with its copies done, the producer CTA (with its pair,
+        // whose copies the consumer prologue's cluster barrier waits for)
+        // takes GEMM tiles from the round's ticket counter like any consumer
+        if (p.join) consumer<PAIR>(p, smem, -1);
     } else {
         consumer<PAIR>(p, smem, blockIdx.x - p.n_producers);
     }

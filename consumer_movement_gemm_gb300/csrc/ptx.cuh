@@ -113,6 +113,38 @@ __device__ __forceinline__ int ld_acquire_cta_smem(const int* p)
     return v;
 }
 
+// Cluster-scope forms for words that the pair's other CTA writes or reads
+// (a CTA pair shares one dynamic tile schedule).
+__device__ __forceinline__ int ld_acquire_cluster_smem(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.cluster.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_add_release_cluster_smem(int* p, int v)
+{
+    asm volatile("red.release.cluster.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// Word of another CTA of the cluster, by its shared::cluster address (mapa).
+__device__ __forceinline__ int ld_acquire_cluster_remote(uint32_t cluster_addr)
+{
+    int v;
+    asm volatile("ld.acquire.cluster.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_remote(uint32_t cluster_addr, int v)
+{
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_cluster_remote(uint32_t cluster_addr, int v)
+{
+    asm volatile("st.release.cluster.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu()
 {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");

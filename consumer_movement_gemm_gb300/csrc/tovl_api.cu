@@ -44,7 +44,7 @@ struct tovl_ctx {
     int producer_mode = 0;     // fused producers: 0 vector copies, 1 staged bulk loads
     int dispatch_align = kBlockRows;  // expert segment alignment: 128, or 256 for CTA-pair tiles
     bool pdl = true;           // programmatic dependent launch between this library's kernels
-    bool role_switch = true;   // reduce-scatter consumers join the reduction after their tiles
+    int role_switch = 1;       // 1: dispatch (single-CTA tiles) and reduce-scatter roles switch; 2: CTA-pair dispatch too
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
     Ctrl ctrl{};
@@ -598,10 +598,10 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.n_nb = N / kTileN;
     p.row_bytes = H * 2;
     int P, C;
-    // role switch (single-CTA tiles): consumer tiles come from the ticket
-    // counter (zeroed by the plan kernel) and producer CTAs take tiles once
-    // their copies are done
-    const bool dyn = h->role_switch && pair == 1;
+    // role switch: consumer tiles (single-CTA or CTA-pair) come from the
+    // ticket counter (zeroed by the plan kernel) and producer CTAs (pairs)
+    // take tiles once their copies are done
+    const bool dyn = pair == 1 ? h->role_switch != 0 : h->role_switch == 2;
     split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
                2.0 * pairs * static_cast<double>(N) * H, pair, dyn);
     p.n_producers = P;
@@ -1003,8 +1003,8 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         h->pdl = value != 0;
         return TOVL_OK;
     case 16:
-        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
-        h->role_switch = value != 0;
+        if (value < 0 || value > 2) return TOVL_ERR_INVALID;
+        h->role_switch = static_cast<int>(value);
         return TOVL_OK;
     case 17:
         if (value != kBlockRows && value != 2 * kBlockRows) return TOVL_ERR_INVALID;
@@ -1034,7 +1034,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 13: *value = h->coop_enabled ? 1 : 0; return TOVL_OK;
     case 14: *value = h->producer_mode; return TOVL_OK;
     case 15: *value = (h->pdl && h->pdl_ok) ? 1 : 0; return TOVL_OK;
-    case 16: *value = h->role_switch ? 1 : 0; return TOVL_OK;
+    case 16: *value = h->role_switch; return TOVL_OK;
     case 17: *value = h->dispatch_align; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }

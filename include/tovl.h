@@ -289,10 +289,13 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * kernel before it -- plan counting, plan finalisation, the fused kernel,
  * combine -- and every kernel waits for its predecessor before it reads
  * memory; 0 = plain stream order; reads back 0 if the device refused it),
- * 16 = role switch (1, the default; 0 = fixed roles): in
- * tovl_dispatch_grouped_gemm consumer tiles are handed out by a ticket
- * counter and producer CTAs take tiles once their copies are done (the
- * automatic split then gives the copy twice its balance share); in
+ * 16 = role switch (1, the default; 0 = fixed roles; 2 = also for CTA-pair
+ * tiles): in tovl_dispatch_grouped_gemm consumer tiles are handed out by a
+ * ticket counter and producer CTAs take tiles once their copies are done
+ * (the automatic split then gives the copy twice its balance share); with
+ * 256-row segments this applies at 2 only (a CTA pair takes one ticket for
+ * both CTAs; measured about 1 % slower than fixed pair roles on the uniform
+ * and Zipf workloads, whose last wave the joining producers cannot fill); in
  * tovl_gemm_reduce_scatter consumer CTAs that have finished their partial
  * tiles take reduction items beside the producer CTAs,
  * 17 = expert segment alignment of tovl_dispatch_grouped_gemm in rows: 128

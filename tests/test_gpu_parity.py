@@ -222,12 +222,15 @@ def test_dispatch_grouped_gemm_small(routing, k_slices, mode, switch):
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
-def test_dispatch_pair_tiles_on_256_row_segments(routing):
+@pytest.mark.parametrize("switch", [1, 2])
+def test_dispatch_pair_tiles_on_256_row_segments(routing, switch):
     # option 17: segments aligned to 256 rows, CTA-pair tiles; the layout is
-    # the oracle's plan with 256-row blocks, the counters stay per 128 rows
+    # the oracle's plan with 256-row blocks, the counters stay per 128 rows.
+    # switch 1: fixed pair roles; 2: one ticket per pair, producer pairs join
     H, N = 192, 512
     with _handle(k_slices=2) as h:
         h.set_option(tovl.OPT_DISPATCH_ALIGN, 256)
+        h.set_option(tovl.OPT_ROLE_SWITCH, switch)
         for r in range(1, 4):
             topk_np, E = ROUTINGS[routing](workloads.round_seed(3, r))
             T, k = topk_np.shape
