@@ -43,27 +43,49 @@ __device__ inline void reducer(const FusedParams& p, int rid)
         const int c0 = s0 / kChunkRows, c1 = (s0 + p.k - 1) / kChunkRows;
         const int* words[2] = {p.ctrl.slot + c0 * S, p.ctrl.slot + c1 * S};
         if (warp_wait_ge(words, c1 != c0 ? 2 : 1, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
-        for (int g = lane; g < groups; g += 32) {
-            float acc[8];
+        // a lane's column groups are lane, lane + 32, ... below N / 8; kBatch
+        // of them are loaded together per staged row, so a token costs k
+        // round trips per batch instead of one per group (a group past the
+        // row loads the lane's first one again and is not stored)
+        constexpr int kBatch = 4;
+        const int per_lane = (groups + 31) / 32;
+        for (int i0 = 0; i0 < per_lane; i0 += kBatch) {
+            float acc[kBatch][8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+            for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[b][c] = 0.0f;
             for (int j = 0; j < p.k; ++j) {
                 const float w = p.gate_w[s0 + j];
-                const int4 v = ptx::ld_v4(reinterpret_cast<const int4*>(staging + (s0 + j) * row_bytes) + g);
-                const uint32_t u[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
-                                       static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+                const int4* row = reinterpret_cast<const int4*>(staging + (s0 + j) * row_bytes);
+                int4 v[kBatch];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(w, bf16_lo(u[c])));
-                    acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(w, bf16_hi(u[c])));
+                for (int b = 0; b < kBatch; ++b) {
+                    const int g = lane + 32 * (i0 + b);
+                    v[b] = ptx::ld_v4(row + (g < groups ? g : lane % groups));
+                }
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const uint32_t u[4] = {static_cast<uint32_t>(v[b].x), static_cast<uint32_t>(v[b].y),
+                                           static_cast<uint32_t>(v[b].z), static_cast<uint32_t>(v[b].w)};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[b][2 * c] = __fadd_rn(acc[b][2 * c], __fmul_rn(w, bf16_lo(u[c])));
+                        acc[b][2 * c + 1] = __fadd_rn(acc[b][2 * c + 1], __fmul_rn(w, bf16_hi(u[c])));
+                    }
                 }
             }
-            int4 o;
-            o.x = static_cast<int>(ptx::pack_bf16x2(acc[0], acc[1]));
-            o.y = static_cast<int>(ptx::pack_bf16x2(acc[2], acc[3]));
-            o.z = static_cast<int>(ptx::pack_bf16x2(acc[4], acc[5]));
-            o.w = static_cast<int>(ptx::pack_bf16x2(acc[6], acc[7]));
-            ptx::st_v4(reinterpret_cast<int4*>(out + static_cast<size_t>(t) * row_bytes) + g, o);
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int g = lane + 32 * (i0 + b);
+                if (g >= groups) break;
+                int4 o;
+                o.x = static_cast<int>(ptx::pack_bf16x2(acc[b][0], acc[b][1]));
+                o.y = static_cast<int>(ptx::pack_bf16x2(acc[b][2], acc[b][3]));
+                o.z = static_cast<int>(ptx::pack_bf16x2(acc[b][4], acc[b][5]));
+                o.w = static_cast<int>(ptx::pack_bf16x2(acc[b][6], acc[b][7]));
+                ptx::st_v4(reinterpret_cast<int4*>(out + static_cast<size_t>(t) * row_bytes) + g, o);
+            }
         }
     }
 }
