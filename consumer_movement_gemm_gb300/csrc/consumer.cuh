@@ -93,7 +93,6 @@ template <int PAIR>
 struct Schedule {
     int unit, n_units, n_tiles;
     uint32_t rank;
-    bool dyn;            // tiles come from the ticket counter through the ring
     __device__ int out_tile(const FusedParams& p, int t) const
     {
         return p.mode == kModeReduceScatter ? t / p.n_shards : t;
@@ -120,7 +119,6 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     sc.unit = cid / PAIR;
     sc.n_units = p.n_consumers / PAIR;
     sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb * (p.mode == kModeReduceScatter ? p.n_shards : 1);
-    sc.dyn = p.dyn != 0;
     return sc;
 }
 
@@ -358,25 +356,17 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
 // the eight rows a quarter-warp writes hit distinct banks), then one lane
 // stores it; rows past the output's extent (the ragged tail of M) are
 // clipped by the store.  The accumulator is released as soon as its last
-// columns are in registers.  The unit's last tile has the operand stages to
-// itself (its MMAs are complete and no load follows), so there each warp
-// stages its four boxes side by side in the A stages and stores them back to
-// back instead of waiting for each store to drain the 2 KB buffer: that
-// epilogue is the one nothing else overlaps.
+// columns are in registers.
 template <int PAIR>
 __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                   uint32_t tmem_base)
 {
-    using T = Tile<PAIR>;
-    constexpr int kBoxes = kTileN / 2 / kEpiBoxCols;
-    static_assert(kEpiWarps * kBoxes * kEpiBufBytes <= T::kStages * T::kStageA,
-                  "the last tile's boxes fit in the A stages");
     const int warp = threadIdx.x / 32;
     const uint32_t lane = ptx::lane_id();
     const int q = warp & 3;
     const int half = (warp - kEpiWarp0) / 4;
     const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
-    const uint8_t* last_buf = s.a + (warp - kEpiWarp0) * kBoxes * kEpiBufBytes;
+    const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
@@ -384,8 +374,7 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        const bool last = t + sc.n_units >= sc.n_tiles;
-        const bool arrived = mbar_wait_backoff(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns, kEpiMaxSleepNs);
+        const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
         if (!__all_sync(0xffffffffu, arrived)) break;
         ptx::tc_fence_after();
         if (p.stats && lane == 0) {
@@ -395,15 +384,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         }
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
 #pragma unroll 1
-        for (int bx = 0; bx < kBoxes; ++bx) {
-            const uint8_t* box = last ? last_buf + bx * kEpiBufBytes : buf;
-            if (!last) {
-                // the previous store from this buffer has finished reading it
-                if (lane == 0) ptx::bulk_wait_read<0>();
-                __syncwarp();
-            }
+        for (int bx = 0; bx < kTileN / 2 / kEpiBoxCols; ++bx) {
+            // the previous store from this buffer has finished reading it
+            if (lane == 0) ptx::bulk_wait_read<0>();
+            __syncwarp();
             {
-                const uint32_t row_addr = ptx::smem_u32(box) + lane * (kEpiBoxCols * 2);
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + bx * kEpiBoxCols, r);
                 ptx::tmem_ld_wait();
@@ -417,7 +402,7 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                                       ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
                 }
             }
-            if (bx == kBoxes - 1) {
+            if (bx == kTileN / 2 / kEpiBoxCols - 1) {
                 // this warp's reads of the accumulator are done: one arrival per warp
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -426,24 +411,12 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                     else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
                 }
             }
-            if (!last) {
-                // the box's generic-proxy writes are visible to the tensor store
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(&p.tmap_out, box, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                      arow + q * 32);
-                    ptx::bulk_commit();
-                }
-            }
-        }
-        if (last) {
+            // the box's generic-proxy writes are visible to the tensor store
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                for (int bx = 0; bx < kBoxes; ++bx)
-                    ptx::tma_store_2d(&p.tmap_out, last_buf + bx * kEpiBufBytes,
-                                      nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols, arow + q * 32);
+                ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                  arow + q * 32);
                 ptx::bulk_commit();
             }
         }
@@ -468,10 +441,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
         }
     }
-    // the stores have read their staging buffers before the CTA retires;
-    // their global writes complete with the grid (a reduce-scatter tile
-    // waited for its writes before it was published)
-    if (lane == 0) ptx::bulk_wait_read<0>();
+    // every store has written global memory before the CTA retires
+    if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();
 }
 
@@ -849,7 +820,7 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
         const int nb = sc.col_block(p, t);
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        const bool arrived = mbar_wait_backoff(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns, kEpiMaxSleepNs);
+        const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
         if (!__all_sync(0xffffffffu, arrived)) break;
         ptx::tc_fence_after();
         if (p.stats && lane == 0) {
@@ -916,16 +887,14 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
         }
     }
-    // the stores have read their staging buffers before the CTA retires;
-    // their global writes complete with the grid (a reduce-scatter tile
-    // waited for its writes before it was published)
-    if (lane == 0) ptx::bulk_wait_read<0>();
+    // every store has written global memory before the CTA retires
+    if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();
 }
 
 }  // namespace dyn
 
-template <int PAIR>
+template <int PAIR, bool DYN>
 __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 {
     using T = Tile<PAIR>;
@@ -971,7 +940,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     ptx::grid_dep_wait();
     const Schedule<PAIR> sc = make_schedule<PAIR>(p, cid);
 
-    if (sc.dyn) {
+    if constexpr (DYN) {
         // role switch: tiles from the ticket counter
         if (warp == 0) dyn::consumer_tma<PAIR, true>(p, s, sc);
         else if (warp == 1) dyn::consumer_mma<PAIR, true>(p, s, sc, tmem_base);

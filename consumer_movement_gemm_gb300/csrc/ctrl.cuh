@@ -23,7 +23,6 @@ constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 5 
 constexpr int kEpiWarp0 = 2;       // first epilogue warp
 constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each owning 128 of the 256 columns
 constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
-constexpr unsigned kEpiMaxSleepNs = 256;   // poll backoff cap of the epilogue's accumulator waits
 constexpr int kTraceCap = 1 << 20; // timeline entries kept when statistics are on
 constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
 constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)

@@ -17,9 +17,11 @@
 // Producers never wait on anyone; consumers wait only on producers, which are
 // resident by construction, and every wait is bounded.
 //
-// Two instantiations: PAIR = 1 (one CTA per 128x256 tile; gather and
-// dispatch) and PAIR = 2 (a cluster pair per 256x256 tile with cta_group::2
-// MMAs; gather).
+// Instantiations: PAIR = 1 (one CTA per 128x256 tile) or 2 (a cluster pair
+// per 256x256 tile with cta_group::2 MMAs), each with a fixed tile schedule
+// or, DYN, the dynamic one of the role switch (tiles from a ticket counter,
+// producers that turn consumer).  The dynamic roles are a kernel of their own
+// so that the fixed-schedule kernel compiles without them.
 #include <cuda_runtime.h>
 #include "ctrl.cuh"
 #include "ptx.cuh"
@@ -31,7 +33,7 @@
 
 namespace tovl {
 
-template <int PAIR>
+template <int PAIR, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ FusedParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -41,9 +43,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         // role switch: with its copies done, the producer CTA (with its pair,
         // whose copies the consumer prologue's cluster barrier waits for)
         // takes GEMM tiles from the round's ticket counter like any consumer
-        if (p.join) consumer<PAIR>(p, smem, -1);
+        if (DYN && p.join) consumer<PAIR, DYN>(p, smem, -1);
     } else {
-        consumer<PAIR>(p, smem, blockIdx.x - p.n_producers);
+        consumer<PAIR, DYN>(p, smem, blockIdx.x - p.n_producers);
     }
 }
 
@@ -77,21 +79,27 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     }
     lc.attrs = attr;
     lc.numAttrs = n;
-    return pair == 2 ? cudaLaunchKernelEx(&lc, fused_kernel<2>, p) : cudaLaunchKernelEx(&lc, fused_kernel<1>, p);
+    if (pair == 2) return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<2, true>, p)
+                                : cudaLaunchKernelEx(&lc, fused_kernel<2, false>, p);
+    return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<1, true>, p) : cudaLaunchKernelEx(&lc, fused_kernel<1, false>, p);
 }
 
 cudaError_t prepare_fused()
 {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+        e = cudaFuncSetAttribute(fused_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
     return e;
 }
 
 int fused_max_active_per_sm()
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kThreads, smem_bytes(1)) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1, false>, kThreads, smem_bytes(1)) != cudaSuccess)
         return 0;
     return n;
 }
@@ -110,7 +118,7 @@ int fused_max_active_pairs()
     lc.attrs = attr;
     lc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fused_kernel<2>, &lc) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fused_kernel<2, false>, &lc) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

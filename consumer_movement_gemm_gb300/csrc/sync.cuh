@@ -115,25 +115,4 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
-// The same wait for waiters off the MMA's critical path (the epilogue warps
-// waiting a whole tile for their accumulator): polls back off with a sleep
-// of up to `max_sleep_ns`, which leaves the SM's issue slots and shared
-// memory to the warps that feed the tensor pipe.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, const Ctrl& ctrl,
-                                                  long long timeout_ns, uint32_t max_sleep_ns)
-{
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t start = ptx::globaltimer();
-    uint32_t sleep_ns = 32;
-    for (uint32_t i = 1;; ++i) {
-        __nanosleep(sleep_ns);
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
-        if ((i & 15) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(timeout_ns)) {
-            record_error(ctrl, kErrTimeout);
-            return false;
-        }
-    }
-}
-
 }  // namespace tovl
