@@ -446,10 +446,10 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     __syncwarp();
 }
 
-// Role switch, dynamic schedule (single CTAs or CTA pairs): the same roles as above,
-// with tiles taken from the round's ticket counter through a shared-memory
-// ring instead of a fixed stride.  Kept apart from the fixed-schedule roles so
-// those compile exactly as they are.
+// Role switch, dynamic schedule (single CTAs or CTA pairs): the same roles as
+// above, with tiles taken from the round's ticket counter through a
+// shared-memory ring instead of a fixed stride.  They are instantiated only in
+// the dynamic-schedule kernels (fused_kernel<PAIR, true>).
 namespace dyn {
 
 // Entries of the ring published so far.  A CTA pair shares one schedule:
