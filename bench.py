@@ -375,9 +375,15 @@ def e2e_tp(h, cfg, W, gathered, out, steps: int, stream):
     t1.record(s_out)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
+    # the last step's downloaded output equals a plain call's on the same input
+    with torch.cuda.stream(stream):
+        h.gather_gemm(X_dev[0], W, gath[0], outs[0], stream=stream)
+    torch.cuda.synchronize()
+    verified = bool(torch.equal(out_host[(steps - 1) % 2], outs[0].cpu()))
     return {"value": cfg.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": X_host.numel() * 2, "d2h_bytes_per_step": out_host[0].numel() * 2,
-            "pipelined": "upload of step i+1 and download of step i-1 overlap step i (two buffer sets, three streams)"}
+            "pipelined": "upload of step i+1 and download of step i-1 overlap step i (two buffer sets, three streams)",
+            "last_output_verified": verified}
 
 
 def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int, align: int = 128):
