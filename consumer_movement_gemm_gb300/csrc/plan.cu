@@ -103,6 +103,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         s_zero = p.force_zero;
         s_bad = p.plan.meta[3];
     }
+    // The routing and in-segment ranks of this thread's first kDstBatch pairs
+    // do not depend on the prefix below: their loads go out with it.
+    constexpr int kDstBatch = 8;
+    int e0[kDstBatch], lr0[kDstBatch];
+#pragma unroll
+    for (int j = 0; j < kDstBatch; ++j) {
+        const int i = j * kPlanThreads + tid;
+        e0[j] = i < p.n_pairs ? p.topk[i] : 0;
+        lr0[j] = i < p.n_pairs ? p.plan.local_rank[i] : 0;
+    }
     // per-expert prefix over segments (each segment's base rank), segments
     // read kPrefixBatch at a time; the previous layout is read alongside
     constexpr int kPrefixBatch = 8;
@@ -164,14 +174,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
     }
     // destination row of every pair and the inverse map, kDstBatch pairs per
     // thread at a time: the routing and in-segment ranks are loaded together
-    constexpr int kDstBatch = 8;
+    // (the first batch's were loaded at the start)
     for (int i0 = 0; i0 < p.n_pairs; i0 += kPlanThreads * kDstBatch) {
         int e[kDstBatch], lr[kDstBatch];
 #pragma unroll
         for (int j = 0; j < kDstBatch; ++j) {
             const int i = i0 + j * kPlanThreads + tid;
-            e[j] = i < p.n_pairs ? p.topk[i] : 0;
-            lr[j] = i < p.n_pairs ? p.plan.local_rank[i] : 0;
+            e[j] = i0 == 0 ? e0[j] : (i < p.n_pairs ? p.topk[i] : 0);
+            lr[j] = i0 == 0 ? lr0[j] : (i < p.n_pairs ? p.plan.local_rank[i] : 0);
         }
 #pragma unroll
         for (int j = 0; j < kDstBatch; ++j) {
