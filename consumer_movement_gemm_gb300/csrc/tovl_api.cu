@@ -547,7 +547,8 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
                                         void* stream)
 {
     if (!h) return TOVL_ERR_INVALID;
-    if (!x || !topk_idx || !W || !dispatched || !expert_offsets || !out) return TOVL_ERR_INVALID;
+    // a round without tokens (T = 0) reads neither x nor topk_idx
+    if (((!x || !topk_idx) && T > 0) || !W || !dispatched || !expert_offsets || !out) return TOVL_ERR_INVALID;
     if (!aligned16(x) || !aligned16(W) || !aligned16(dispatched) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
         return TOVL_ERR_INVALID;
@@ -736,6 +737,7 @@ TOVL_API int tovl_combine(tovl_handle h, const void* y, int N, const float* gate
     if (N > kMaxK) return TOVL_ERR_UNSUPPORTED;
     const long long pairs = static_cast<long long>(h->last_T) * h->last_k;
     if (pairs > h->cfg.max_rows) return TOVL_ERR_INVALID;
+    if (pairs == 0) return TOVL_OK;    // the last dispatch round had no tokens: nothing to combine, no round
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     FusedParams p;

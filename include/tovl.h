@@ -121,8 +121,10 @@ long long tovl_dispatch_rows_aligned(int T, int k, int E, int align);
 /* Dispatch scatter of top-k routed tokens into padded per-expert segments,
  * followed by a grouped GEMM per expert (notify-stage counting of the DeepEP
  * FIFO-pipeline page; row-block counters with padding seeds of section 5).
- *   x           device, bf16 [T][H]
+ *   x           device, bf16 [T][H] (may be null when T = 0)
  *   topk_idx    device, int32 [T][k]: expert of pair (t, j), each in [0, E)
+ *               (may be null when T = 0: a round without tokens, whose plan
+ *               is empty and whose call still counts as one round)
  *   H           multiple of 64, at most 32768 (the GEMM K)
  *   W           device, bf16 [E][H][N], N multiple of 256
  *   dispatched  device, bf16 [tovl_dispatch_rows(T,k,E)][H]: rows of expert e
@@ -181,9 +183,11 @@ int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shards, int M
  * T, k and the routing plan are the last dispatch call's; T*k <= max_rows.
  * Without an earlier dispatch on the handle the call returns
  * TOVL_ERR_INVALID; after a dispatch whose plan was rejected (bad expert id)
- * the round is a no-op that sets TOVL_ERR_INVALID in the status word.  One
- * round (one sequence number), like the other calls.  Option 1 (producer
- * CTAs) applies; the remaining SMs reduce (default: half and half). */
+ * the round is a no-op that sets TOVL_ERR_INVALID in the status word; after
+ * a dispatch round without tokens (T = 0) the call returns TOVL_OK and does
+ * nothing (no round).  Otherwise one round (one sequence number), like the
+ * other calls.  Option 1 (producer CTAs) applies; the remaining SMs reduce
+ * (default: 7/12 of the SMs copy). */
 int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void* staging, void* combined,
                  void* stream);
 

@@ -489,3 +489,88 @@ def test_gated_copy_small(row_bytes, copy_mode):
         assert h.sync_status() == 0
         assert torch.equal(dst2, dst)
         _check_ctrl(h, 2)
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_dispatch_round_then_normal_rounds():
+    # T = 0: a round without routed pairs; the plan is empty, nothing is
+    # copied or computed, and the next rounds are normal
+    H, N, E = 64, 256, 3
+    with _handle() as h:
+        x0 = torch.zeros(0, H, dtype=torch.bfloat16, device=DEV)
+        W = workloads.bf16_normal((E, H, N), 1.0, 61, DEV)
+        topk0 = np.zeros((0, 2), np.int32)
+        dispatched, offs, out = _dispatch_round(h, x0, topk0, W)
+        assert h.sync_status() == 0
+        counts, dst, src, pad, blk, m_pad = h.read_plan(0, 2, E)
+        assert m_pad == 0 and np.array_equal(counts, np.zeros(E, np.int32))
+        assert np.array_equal(offs.cpu().numpy(), np.zeros(E + 1, np.int32))
+        _check_ctrl(h, 1)
+        for r in (2, 3):
+            topk_np = workloads.uniform_topk(90, 2, E, r)
+            x = workloads.bf16_normal((90, H), 1.0, 60 + r, DEV)
+            dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+            assert h.sync_status() == 0
+            _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
+
+
+def test_combine_after_empty_dispatch_is_a_no_op():
+    H, N, E = 64, 256, 3
+    with _handle() as h:
+        _dispatch_round(h, torch.zeros(0, H, dtype=torch.bfloat16, device=DEV), np.zeros((0, 2), np.int32),
+                        workloads.bf16_normal((E, H, N), 1.0, 62, DEV))
+        y = workloads.bf16_normal((256, N), 1.0, 63, DEV)
+        staging = torch.full((1, N), 5.0, dtype=torch.bfloat16, device=DEV)
+        combined = torch.full((1, N), 5.0, dtype=torch.bfloat16, device=DEV)
+        h.combine(y, torch.ones(1, dtype=torch.float32, device=DEV), staging, combined)
+        assert h.sync_status() == 0
+        assert torch.all(combined == 5.0) and torch.all(staging == 5.0)
+        _check_ctrl(h, 1)
+
+
+def test_gated_copy_rejects_zero_rows():
+    with _handle(max_rows=64) as h:
+        src = torch.zeros(1, 64, dtype=torch.uint8, device=DEV)
+        perm = torch.zeros(1, dtype=torch.int32, device=DEV)
+        with pytest.raises(tovl.TovlError):
+            h.gated_copy(src[:0], src[:0], perm[:0])
+        assert h.sync_status() == 0
+
+
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gather_gemm_widest_rows(pairs):
+    # K = 32768, the largest supported row (one 64 KB row per producer pass)
+    cfg = workloads.GatherCfg("widest", 2, 64, 32768, 256, rounds=1)
+    with _handle(producer_ctas=4, k_slices=1) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
+        X, W, gathered, out = _gather_round(h, cfg, 71)
+        assert h.sync_status() == 0
+        G = oracle.gather([bits(X[s]) for s in range(cfg.shards)])
+        assert np.array_equal(bits(gathered), G)
+        assert_close(out, oracle.matmul_f32(G, bits(W)), "K = 32768")
+        _check_ctrl(h, 1)
+
+
+def test_gather_gemm_most_shards():
+    # 64 shards (the most a call takes) of 24 rows each: chunks span shards
+    cfg = workloads.GatherCfg("many shards", 64, 24, 128, 256, rounds=1)
+    with _handle(producer_ctas=8, k_slices=2) as h:
+        X, W, gathered, out = _gather_round(h, cfg, 72)
+        assert h.sync_status() == 0
+        G = oracle.gather([bits(X[s]) for s in range(cfg.shards)])
+        assert np.array_equal(bits(gathered), G)
+        assert_close(out, oracle.matmul_f32(G, bits(W)), "64 shards")
+        _check_ctrl(h, 1)
+
+
+def test_dispatch_most_experts():
+    # 512 experts (the most a call takes), most of them empty or with one row
+    H, N, E = 64, 256, 512
+    with _handle(max_experts=E, max_rows=1 << 17) as h:
+        for r in (1, 2):
+            topk_np = workloads.uniform_topk(300, 2, E, 80 + r)
+            x = workloads.bf16_normal((300, H), 1.0, 82 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1.0, 84 + r, DEV)
+            dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+            assert h.sync_status() == 0
+            _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
