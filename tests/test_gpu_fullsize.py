@@ -49,11 +49,15 @@ def _on(t: torch.Tensor, rows: np.ndarray) -> torch.Tensor:
 
 
 def test_tp_gather_gemm_full_size():
-    # 4 shards x 768 rows, K = N = 4096: the handle bench.py times the TP
-    # step with (automatic producer / consumer split, CTA pairs, 4 K-slices)
+    # 4 shards x 768 rows, K = N = 4096, the configuration's 20 rounds with
+    # new inputs every round and sequences never reset: the handle bench.py
+    # times the TP step with (automatic producer / consumer split, CTA pairs,
+    # 4 K-slices)
     cfg = workloads.TP
+    R = cfg.rows_per_shard
+    must = [0, 127, 128, 255, 256, R - 1, R, 2 * R - 1, 2 * R, cfg.M - 129, cfg.M - 128, cfg.M - 1]
     with tovl.Handle(0, max_rows=1 << 14, k_slices=4) as h:
-        for r in (1, 2):
+        for r in range(1, cfg.rounds + 1):
             X, W = workloads.gather_inputs(cfg, workloads.round_seed(cfg.seed, r), DEV)
             gathered = torch.full((cfg.M, cfg.K), 3.0, dtype=torch.bfloat16, device=DEV)
             out = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=DEV)
@@ -61,53 +65,58 @@ def test_tp_gather_gemm_full_size():
             assert h.sync_status() == 0
             G = oracle.gather([bits(X[s]) for s in range(cfg.shards)])
             assert np.array_equal(bits(gathered), G), f"gathered buffer, round {r}"
-            R = cfg.rows_per_shard
-            must = [0, 127, 128, 255, 256, R - 1, R, 2 * R - 1, 2 * R, cfg.M - 129, cfg.M - 128, cfg.M - 1]
-            rows = _rows(cfg.M, must, 36, r)
+            rows = _rows(cfg.M, must if r in (1, cfg.rounds) else [], 36 if r in (1, cfg.rounds) else 6, r)
             assert_close(_on(out, rows), oracle.matmul_rows_f32(G, bits(W), rows), f"TP output rows, round {r}")
             _check_ctrl(h, r)
+
+
+def _dispatch_full_round(h, cfg, align, r, dispatched, offs, out):
+    x, topk_np, W = workloads.dispatch_inputs(cfg, r - 1, DEV)
+    h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
+    assert h.sync_status() == 0
+    p = oracle.dispatch_plan(topk_np, cfg.E, block_rows=align)
+    counts, dst, src, pad, blk, m_pad = h.read_plan(cfg.T, cfg.k, cfg.E)
+    assert m_pad == p.m_pad
+    assert np.array_equal(counts, p.counts)
+    assert np.array_equal(offs.cpu().numpy(), p.off)
+    assert np.array_equal(dst, p.dst)
+    assert np.array_equal(src, p.src)
+    # per 128-row block: padding = rows without a source, expert = segment
+    real = (p.src >= 0).reshape(-1, 128).sum(axis=1)
+    assert np.array_equal(pad, 128 - real)
+    assert np.array_equal(blk, np.searchsorted(p.off, np.arange(0, m_pad, 128), side="right") - 1)
+    D = oracle.dispatch(bits(x), p.dst, cfg.k, p.m_pad)
+    assert np.array_equal(bits(dispatched[:m_pad]), D), f"dispatched buffer, round {r}"
+    # sampled real rows of every expert (its first and last row among them)
+    for e in range(cfg.E):
+        lo, n_e = int(p.off[e]), int(p.counts[e])
+        if n_e == 0:
+            continue
+        rows = _rows(n_e, [0, n_e - 1], 2, e) + lo
+        assert_close(_on(out, rows), oracle.matmul_rows_f32(D, bits(W[e]), rows), f"expert {e}, round {r}")
+    # padding rows of the output are exact zeros
+    pad_rows = np.nonzero(p.src < 0)[0]
+    if pad_rows.size:
+        assert torch.count_nonzero(_on(out, pad_rows)) == 0
+    _check_ctrl(h, r)
 
 
 @pytest.mark.parametrize("name,align", [("DISPATCH", 128), ("DISPATCH", 256), ("SKEWED", 128), ("SKEWED", 256)])
 def test_dispatch_grouped_gemm_full_size(name, align):
     # uniform top-2 of 8 (T=4096, H=4096) and Zipf(1.2) top-4 of 32 (T=8192,
     # H=7168), N=2048; 128-row segments (single-CTA tiles, role switch) and
-    # 256-row segments (CTA pairs): the handles bench.py's dispatch lines use
+    # 256-row segments (CTA pairs): the handles bench.py's dispatch lines
+    # use.  Three rounds with a new routing each (the padding rows move
+    # between rounds and must be zero again), sequences never reset.
     cfg = getattr(workloads, name)
-    x, topk_np, W = workloads.dispatch_inputs(cfg, 0, DEV)
     rows_cap = tovl.dispatch_rows_aligned(cfg.T, cfg.k, cfg.E, align)
     with tovl.Handle(0, max_rows=rows_cap, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=4) as h:
         h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
         dispatched = torch.full((rows_cap, cfg.H), 3.0, dtype=torch.bfloat16, device=DEV)
         offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
         out = torch.empty(rows_cap, cfg.N, dtype=torch.bfloat16, device=DEV)
-        h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
-        assert h.sync_status() == 0
-        p = oracle.dispatch_plan(topk_np, cfg.E, block_rows=align)
-        counts, dst, src, pad, blk, m_pad = h.read_plan(cfg.T, cfg.k, cfg.E)
-        assert m_pad == p.m_pad
-        assert np.array_equal(counts, p.counts)
-        assert np.array_equal(offs.cpu().numpy(), p.off)
-        assert np.array_equal(dst, p.dst)
-        assert np.array_equal(src, p.src)
-        # per 128-row block: padding = rows without a source, expert = segment
-        real = (p.src >= 0).reshape(-1, 128).sum(axis=1)
-        assert np.array_equal(pad, 128 - real)
-        assert np.array_equal(blk, np.searchsorted(p.off, np.arange(0, m_pad, 128), side="right") - 1)
-        D = oracle.dispatch(bits(x), p.dst, cfg.k, p.m_pad)
-        assert np.array_equal(bits(dispatched[:m_pad]), D), "dispatched buffer"
-        # sampled real rows of every expert (its first and last row among them)
-        for e in range(cfg.E):
-            lo, n_e = int(p.off[e]), int(p.counts[e])
-            if n_e == 0:
-                continue
-            rows = _rows(n_e, [0, n_e - 1], 2, e) + lo
-            assert_close(_on(out, rows), oracle.matmul_rows_f32(D, bits(W[e]), rows), f"{name} expert {e}")
-        # padding rows of the output are exact zeros
-        pad_rows = np.nonzero(p.src < 0)[0]
-        if pad_rows.size:
-            assert torch.count_nonzero(_on(out, pad_rows)) == 0
-        _check_ctrl(h, 1)
+        for r in (1, 2, 3):
+            _dispatch_full_round(h, cfg, align, r, dispatched, offs, out)
 
 
 def test_combine_full_size():
@@ -153,25 +162,48 @@ def test_gemm_reduce_scatter_full_size():
         _check_ctrl(h, 1)
 
 
-def test_gated_copy_full_size():
-    # 2^20 permuted 8 KB rows (8 GiB each way), the copy line's handle
+@pytest.mark.parametrize("row_bytes", [256, 1024, 8192, 16384])
+def test_gated_copy_full_size(row_bytes):
+    # 2^20 permuted rows (256 B - 16 KB, up to 16 GiB each way), the copy
+    # line's handle and copy mode, two rounds
     cfg = workloads.COPY
-    n, rb = cfg.n_rows, 8192
+    n, rb = cfg.n_rows, row_bytes
     perm_np = workloads.permutation(n, cfg.seed)
+    perm = torch.from_numpy(perm_np).to(DEV)
+    rows = _rows(n, [0, n - 1], 2048, 7)
+    dests = perm_np[rows].astype(np.int64)
+    rank = np.argsort(np.argsort(dests)).astype(np.int32)
     with tovl.Handle(0, max_rows=n) as h:
         src = torch.empty(n, rb, dtype=torch.uint8, device=DEV)
-        src.random_(0, 256)
         dst = torch.zeros_like(src)
-        h.gated_copy(src, dst, torch.from_numpy(perm_np).to(DEV), gated=True)
-        assert h.sync_status() == 0
-        # a sample of source rows, as a smaller copy for the oracle: row j of
-        # the sample goes to the rank of its destination among the sample's
-        rows = _rows(n, [0, n - 1], 2048, 7)
-        dests = perm_np[rows].astype(np.int64)
-        rank = np.argsort(np.argsort(dests)).astype(np.int32)
-        want = oracle.copy_perm(_on(src, rows).cpu().numpy(), rank)
-        got = _on(dst, np.sort(dests)).cpu().numpy()
-        assert np.array_equal(got, want), "sampled destination rows"
-        _check_ctrl(h, 1)
+        for r in (1, 2):
+            src.random_(0, 256)
+            h.gated_copy(src, dst, perm, gated=True)
+            assert h.sync_status() == 0
+            # the sample of source rows as a smaller copy for the oracle: row j
+            # of the sample goes to the rank of its destination in the sample
+            want = oracle.copy_perm(_on(src, rows).cpu().numpy(), rank)
+            got = _on(dst, np.sort(dests)).cpu().numpy()
+            assert np.array_equal(got, want), f"sampled destination rows, round {r}"
+            _check_ctrl(h, r)
         del src, dst
         torch.cuda.empty_cache()
+
+
+def test_gated_copy_thousand_rounds():
+    # the sweep's 1000 rounds of monotonic sequence numbers (256 B rows):
+    # the control plane's closed form after every 100th round and the data of
+    # the last round
+    cfg = workloads.COPY
+    n, rb = cfg.n_rows, 256
+    perm_np = workloads.permutation(n, cfg.seed)
+    perm = torch.from_numpy(perm_np).to(DEV)
+    with tovl.Handle(0, max_rows=n) as h:
+        src = workloads.random_bytes(n, rb, 3, DEV)
+        dst = torch.zeros_like(src)
+        for r in range(1, cfg.rounds + 1):
+            h.gated_copy(src, dst, perm, gated=True)
+            if r % 100 == 0:
+                assert h.sync_status() == 0
+                _check_ctrl(h, r)
+        assert np.array_equal(dst.cpu().numpy(), oracle.copy_perm(src.cpu().numpy(), perm_np))
