@@ -332,6 +332,26 @@ def acceptance(h, timer, cfg, X, W, gathered, out, n: int, producers: int):
     }
 
 
+def unfused_context(timer, cfg, X, W, n: int):
+    """For context only, not the product path: the same step without fusion,
+    with library kernels on the same GPU -- a torch copy of the shards into
+    the gathered buffer (every SM) and a cuBLAS GEMM (torch.matmul), alone
+    and back to back (median ms, L2 flushed before each)."""
+    import torch
+    G = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device="cuda")
+    C = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device="cuda")
+    Xf = X.reshape(cfg.M, cfg.K)
+    copy = lambda: G.copy_(Xf)  # noqa: E731
+    gemm = lambda: torch.matmul(G, W, out=C)  # noqa: E731
+    both = lambda: (copy(), gemm())  # noqa: E731
+    res = {}
+    for name, fn in (("torch_copy_ms", copy), ("cublas_gemm_ms", gemm), ("copy_then_cublas_ms", both)):
+        timer.time_calls(fn, 3)
+        res[name] = statistics.median(timer.time_calls(fn, n))
+    res["note"] = "library kernels on the same GPU for comparison; not part of the timed product path"
+    return res
+
+
 def e2e_tp(h, cfg, W, gathered, out, steps: int, stream):
     """Host shards -> device, fused call, device -> host output, every step.
     Pipelined like a serving loop: two buffer sets and three streams, so the
@@ -555,6 +575,7 @@ def run_tovl(args):
 
     acc = acceptance(h, timer, cfg, X, W, gathered, out, 50, args.producers)
     e2e = e2e_tp(h, cfg, W, gathered, out, 50, stream)
+    context = unfused_context(timer, cfg, X, W, 30)
 
     extra = {}
     if args.sweep:
@@ -608,6 +629,7 @@ def run_tovl(args):
         "gated_copy_GBps": (max(r["gated_GBps"] for r in extra["gated_copy"]["sweep"])
                             if "gated_copy" in extra else None),
         "acceptance": acc,
+        "unfused_context": context,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                      "traffic": traffic, "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
                      "frac_of_sustained": tf / peaks.get("bf16_tflops_sustained", peak)},
