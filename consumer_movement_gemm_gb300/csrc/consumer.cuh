@@ -894,7 +894,27 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
 
 }  // namespace dyn
 
-template <int PAIR, bool DYN>
+// Embedded producers: in a launch without producer CTAs, the consumer CTAs'
+// warps past the gate warp (5 per CTA) copy the rows, with the producers'
+// item order, counters and seeds (producer.cuh), dealt across every CTA.
+__device__ __forceinline__ void embedded_producer(const FusedParams& p)
+{
+    constexpr int kFirst = kGateWarp + 1;
+    constexpr int kCopyWarps = kThreads / 32 - kFirst;
+    const int warp = threadIdx.x / 32;
+    const int gw = (warp - kFirst) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+    const int n_gw = kCopyWarps * static_cast<int>(gridDim.x);
+    if (warp == kFirst && ptx::lane_id() == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
+    seed_counters(p, gw, n_gw, true);
+    if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
+    else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
+    else copy_items<4>(p, gw, n_gw);
+    seed_counters(p, gw, n_gw, false);
+    __syncwarp();
+    if (ptx::lane_id() == 0) stat_max(p, kStatProdEndNs, ptx::globaltimer());
+}
+
+template <int PAIR, bool DYN, bool EMB>
 __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 {
     using T = Tile<PAIR>;
@@ -951,6 +971,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
+        else if (EMB && warp > kGateWarp) embedded_producer(p);
     }
     __syncwarp();
 

@@ -19,7 +19,7 @@ constexpr int kTileN = 256;
 constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 5 idle (consumers) / 16 copy warps (producers)
+constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 5 spare (consumers) / 16 copy warps (producers)
 constexpr int kEpiWarp0 = 2;       // first epilogue warp
 constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each owning 128 of the 256 columns
 constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
@@ -152,6 +152,7 @@ struct FusedParams {
     int rs_join;          // consumers take reduction items once their tiles are done (role switch)
     int dyn;              // consumer tiles handed out by a ticket counter (ctrl.work, zeroed by the plan kernel)
     int join;             // producer CTAs become consumers once their copies are done (role switch)
+    int embedded;         // no producer CTAs: the consumer CTAs' spare warps copy the rows
     void* rs_out;         // [M][N] bf16
     // destinations
     void* gathered;       // gathered / dispatched buffer

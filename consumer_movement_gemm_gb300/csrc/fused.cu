@@ -20,8 +20,10 @@
 // Instantiations: PAIR = 1 (one CTA per 128x256 tile) or 2 (a cluster pair
 // per 256x256 tile with cta_group::2 MMAs), each with a fixed tile schedule
 // or, DYN, the dynamic one of the role switch (tiles from a ticket counter,
-// producers that turn consumer).  The dynamic roles are a kernel of their own
-// so that the fixed-schedule kernel compiles without them.
+// producers that turn consumer); and, EMB, a fixed schedule without producer
+// CTAs whose consumer CTAs copy the rows in their spare warps.  Each variant
+// is a kernel of its own so that the fixed-schedule kernel compiles without
+// the others' roles.
 #include <cuda_runtime.h>
 #include "ctrl.cuh"
 #include "ptx.cuh"
@@ -33,7 +35,7 @@
 
 namespace tovl {
 
-template <int PAIR, bool DYN>
+template <int PAIR, bool DYN, bool EMB>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ FusedParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -43,9 +45,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         // role switch: with its copies done, the producer CTA (with its pair,
         // whose copies the consumer prologue's cluster barrier waits for)
         // takes GEMM tiles from the round's ticket counter like any consumer
-        if (DYN && p.join) consumer<PAIR, DYN>(p, smem, -1);
+        if (DYN && p.join) consumer<PAIR, DYN, false>(p, smem, -1);
     } else {
-        consumer<PAIR, DYN>(p, smem, blockIdx.x - p.n_producers);
+        consumer<PAIR, DYN, EMB>(p, smem, blockIdx.x - p.n_producers);
     }
 }
 
@@ -79,27 +81,35 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     }
     lc.attrs = attr;
     lc.numAttrs = n;
-    if (pair == 2) return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<2, true>, p)
-                                : cudaLaunchKernelEx(&lc, fused_kernel<2, false>, p);
-    return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<1, true>, p) : cudaLaunchKernelEx(&lc, fused_kernel<1, false>, p);
+    if (p.embedded)
+        return pair == 2 ? cudaLaunchKernelEx(&lc, fused_kernel<2, false, true>, p)
+                         : cudaLaunchKernelEx(&lc, fused_kernel<1, false, true>, p);
+    if (pair == 2) return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<2, true, false>, p)
+                                : cudaLaunchKernelEx(&lc, fused_kernel<2, false, false>, p);
+    return p.dyn ? cudaLaunchKernelEx(&lc, fused_kernel<1, true, false>, p)
+                 : cudaLaunchKernelEx(&lc, fused_kernel<1, false, false>, p);
 }
 
 cudaError_t prepare_fused()
 {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+        e = cudaFuncSetAttribute(fused_kernel<1, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+        e = cudaFuncSetAttribute(fused_kernel<2, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+        e = cudaFuncSetAttribute(fused_kernel<2, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
     return e;
 }
 
 int fused_max_active_per_sm()
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1, false>, kThreads, smem_bytes(1)) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1, false, false>, kThreads, smem_bytes(1)) != cudaSuccess)
         return 0;
     return n;
 }
@@ -118,7 +128,7 @@ int fused_max_active_pairs()
     lc.attrs = attr;
     lc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fused_kernel<2, false>, &lc) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fused_kernel<2, false, false>, &lc) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

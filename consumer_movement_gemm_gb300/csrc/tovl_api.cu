@@ -45,6 +45,7 @@ struct tovl_ctx {
     int dispatch_align = kBlockRows;  // expert segment alignment: 128, or 256 for CTA-pair tiles
     bool pdl = true;           // programmatic dependent launch between this library's kernels
     int role_switch = 1;       // 1: dispatch (single-CTA tiles) and reduce-scatter roles switch; 2: CTA-pair dispatch too
+    int embedded = 1;          // without producer CTAs, the consumer CTAs' spare warps copy: 1 dispatch, 2 also gather
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
     Ctrl ctrl{};
@@ -479,6 +480,19 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     p.n_producers = (flags & 1) ? P : 0;
     p.n_consumers = (flags & 2) ? C : 0;
     p.gated = (flags & 4) ? 1 : 0;
+    if (h->embedded == 2 && flags == (1 | 2 | 4)) {
+        // the fused call without producer CTAs: every SM (co-resident pair)
+        // a consumer, the copy in the consumer CTAs' spare warps
+        C = (pair == 2 && 2 * h->max_pairs < h->num_sms) ? 2 * h->max_pairs : h->num_sms;
+        if (h->consumers > 0 && h->consumers < C) C = h->consumers;
+        if (pair == 2) C &= ~1;
+        P = 0;
+        h->last_P = P;
+        h->last_C = C;
+        p.n_producers = 0;
+        p.n_consumers = C;
+        p.embedded = 1;
+    }
     call_geometry(h, p, C, split_pair);
     p.n_shards = S;
     p.rows_per_shard = R;
@@ -602,14 +616,27 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     // role switch: consumer tiles (single-CTA or CTA-pair) come from the
     // ticket counter (zeroed by the plan kernel) and producer CTAs (pairs)
     // take tiles once their copies are done
-    const bool dyn = pair == 1 ? h->role_switch != 0 : h->role_switch == 2;
-    split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
-               2.0 * pairs * static_cast<double>(N) * H, pair, dyn);
+    const bool emb = h->embedded != 0;
+    const bool dyn = !emb && (pair == 1 ? h->role_switch != 0 : h->role_switch == 2);
+    if (emb) {
+        // every SM a consumer (CTA pairs: every co-resident pair); the copy
+        // runs in the consumer CTAs' spare warps
+        P = 0;
+        C = (pair == 2 && 2 * h->max_pairs < h->num_sms) ? 2 * h->max_pairs : h->num_sms;
+        if (h->consumers > 0 && h->consumers < C) C = h->consumers;
+        if (pair == 2) C &= ~1;
+        h->last_P = P;
+        h->last_C = C;
+    } else {
+        split_ctas(h, P, C, static_cast<int>(rows / kTileM), p.n_nb, 4.0 * pairs * H,
+                   2.0 * pairs * static_cast<double>(N) * H, pair, dyn);
+    }
     p.n_producers = P;
     p.n_consumers = C;
     p.gated = 1;
     p.dyn = dyn ? 1 : 0;
     p.join = dyn ? 1 : 0;
+    p.embedded = emb ? 1 : 0;
     call_geometry(h, p, C, pair);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;
@@ -1014,6 +1041,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value != kBlockRows && value != 2 * kBlockRows) return TOVL_ERR_INVALID;
         h->dispatch_align = static_cast<int>(value);
         return TOVL_OK;
+    case 18:
+        if (value < 0 || value > 2) return TOVL_ERR_INVALID;
+        h->embedded = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -1040,6 +1071,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 15: *value = (h->pdl && h->pdl_ok) ? 1 : 0; return TOVL_OK;
     case 16: *value = h->role_switch; return TOVL_OK;
     case 17: *value = h->dispatch_align; return TOVL_OK;
+    case 18: *value = h->embedded; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

@@ -41,6 +41,7 @@ OPT_PRODUCER_MODE = 14
 OPT_PDL = 15
 OPT_ROLE_SWITCH = 16
 OPT_DISPATCH_ALIGN = 17
+OPT_EMBEDDED = 18
 
 
 class TovlError(RuntimeError):

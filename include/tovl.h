@@ -294,8 +294,9 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * combine -- and every kernel waits for its predecessor before it reads
  * memory; 0 = plain stream order; reads back 0 if the device refused it),
  * 16 = role switch (1, the default; 0 = fixed roles; 2 = also for CTA-pair
- * tiles): in tovl_dispatch_grouped_gemm consumer tiles are handed out by a
- * ticket counter and producer CTAs take tiles once their copies are done
+ * tiles): in tovl_dispatch_grouped_gemm with producer CTAs (option 18 = 0)
+ * consumer tiles are handed out by a ticket counter and producer CTAs take
+ * tiles once their copies are done
  * (the automatic split then gives the copy twice its balance share); with
  * 256-row segments this applies at 2 only (a CTA pair takes one ticket for
  * both CTAs; measured about 1 % slower than fixed pair roles on the uniform
@@ -308,6 +309,14 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * 256-row tiles inside one expert; the padded rows are zero and their
  * block counters are seeded like any padding; buffers then need
  * tovl_dispatch_rows_aligned(T, k, E, 256) rows),
+ * 18 = embedded producers (1, the default: in tovl_dispatch_grouped_gemm;
+ * 2 = also in tovl_gather_gemm; 0 = off): the call launches no producer
+ * CTAs; every SM (every co-resident CTA pair) is a consumer and the
+ * consumer CTAs' five spare warps copy the rows, in the producers' order and
+ * with their counters and seeds (16-byte vector copies whatever option 14
+ * says; the role switch does not apply).  Measured on GB300: dispatch 6-9 %
+ * faster (a wave fewer of expert tiles), the TP gather 6 % slower (its three
+ * tile waves stay three; the copy warps share the SMs),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

@@ -102,16 +102,18 @@ def _dispatch_full_round(h, cfg, align, r, dispatched, offs, out):
 
 
 @pytest.mark.parametrize("name,align", [("DISPATCH", 128), ("DISPATCH", 256), ("SKEWED", 128), ("SKEWED", 256)])
-def test_dispatch_grouped_gemm_full_size(name, align):
+@pytest.mark.parametrize("embedded", [1, 0])
+def test_dispatch_grouped_gemm_full_size(name, align, embedded):
     # uniform top-2 of 8 (T=4096, H=4096) and Zipf(1.2) top-4 of 32 (T=8192,
     # H=7168), N=2048; 128-row segments (single-CTA tiles, role switch) and
-    # 256-row segments (CTA pairs): the handles bench.py's dispatch lines
-    # use.  Three rounds with a new routing each (the padding rows move
+    # 256-row segments (CTA pairs), with embedded producers (the default) and
+    # with producer CTAs: the handles bench.py's dispatch lines use.  Three rounds with a new routing each (the padding rows move
     # between rounds and must be zero again), sequences never reset.
     cfg = getattr(workloads, name)
     rows_cap = tovl.dispatch_rows_aligned(cfg.T, cfg.k, cfg.E, align)
     with tovl.Handle(0, max_rows=rows_cap, max_pairs=cfg.T * cfg.k, max_experts=cfg.E, k_slices=4) as h:
         h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
+        h.set_option(tovl.OPT_EMBEDDED, embedded)   # 1: the default, copy warps in the consumer CTAs
         dispatched = torch.full((rows_cap, cfg.H), 3.0, dtype=torch.bfloat16, device=DEV)
         offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
         out = torch.empty(rows_cap, cfg.N, dtype=torch.bfloat16, device=DEV)

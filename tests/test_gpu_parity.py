@@ -209,6 +209,7 @@ def test_dispatch_grouped_gemm_small(routing, k_slices, mode, switch):
     # consumer (1), or the static schedule (0)
     H, N = 192, 256
     with _handle(k_slices=k_slices) as h:
+        h.set_option(tovl.OPT_EMBEDDED, 0)      # producer CTAs (the embedded copy has its own test)
         h.set_option(tovl.OPT_PRODUCER_MODE, mode)
         h.set_option(tovl.OPT_ROLE_SWITCH, switch)
         for r in range(1, 4):
@@ -229,6 +230,7 @@ def test_dispatch_pair_tiles_on_256_row_segments(routing, switch):
     # switch 1: fixed pair roles; 2: one ticket per pair, producer pairs join
     H, N = 192, 512
     with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_EMBEDDED, 0)      # producer CTAs (the embedded copy has its own test)
         h.set_option(tovl.OPT_DISPATCH_ALIGN, 256)
         h.set_option(tovl.OPT_ROLE_SWITCH, switch)
         for r in range(1, 4):
@@ -574,3 +576,37 @@ def test_dispatch_most_experts():
             dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
             assert h.sync_status() == 0
             _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
+
+
+@pytest.mark.parametrize("routing", list(ROUTINGS))
+@pytest.mark.parametrize("align", [128, 256])
+def test_dispatch_embedded_producers(routing, align):
+    # option 18: no producer CTAs; the consumer CTAs' spare warps copy the
+    # rows; the same plan, buffers and counters as with producer CTAs
+    H, N = 192, 512
+    with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
+        h.set_option(tovl.OPT_EMBEDDED, 1)
+        assert h.get_option(tovl.OPT_EMBEDDED) == 1
+        for r in range(1, 4):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(4, r))
+            T, k = topk_np.shape
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 960 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 970 + r, DEV)
+            rows = tovl.dispatch_rows_aligned(T, k, E, align)
+            dispatched = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device=DEV)
+            offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+            out = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+            h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
+            assert h.sync_status() == 0
+            assert h.get_option(tovl.OPT_PRODUCERS) == 0
+            p = oracle.dispatch_plan(topk_np, E, block_rows=align)
+            counts, dst, src, pad, blk, m_pad = h.read_plan(T, k, E)
+            assert m_pad == p.m_pad
+            assert np.array_equal(offs.cpu().numpy(), p.off)
+            assert np.array_equal(dst, p.dst)
+            assert np.array_equal(src, p.src)
+            D = oracle.dispatch(bits(x), p.dst, k, p.m_pad)
+            assert np.array_equal(bits(dispatched[:m_pad]), D), "dispatched buffer"
+            assert_close(out[:m_pad], oracle.grouped_matmul_f32(D, bits(W), p.off), "embedded producers")
+            _check_ctrl(h, r)
