@@ -897,14 +897,21 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
 // Embedded producers: in a launch without producer CTAs, the consumer CTAs'
 // warps past the gate warp (5 per CTA) copy the rows, with the producers'
 // item order, counters and seeds (producer.cuh), dealt across every CTA.
+// They own no mbarrier, TMEM column or ring entry, so they skip the
+// prologue: they count toward its barrier without waiting for it and start
+// as soon as the previous kernel's output (the plan) is visible.
+constexpr int kFirstCopyWarp = kGateWarp + 1;
+
+template <int PAIR>
 __device__ __forceinline__ void embedded_producer(const FusedParams& p)
 {
-    constexpr int kFirst = kGateWarp + 1;
-    constexpr int kCopyWarps = kThreads / 32 - kFirst;
+    constexpr int kCopyWarps = kThreads / 32 - kFirstCopyWarp;
     const int warp = threadIdx.x / 32;
-    const int gw = (warp - kFirst) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+    if (PAIR == 2) ptx::cluster_arrive_relaxed();
+    ptx::grid_dep_wait();
+    const int gw = (warp - kFirstCopyWarp) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
     const int n_gw = kCopyWarps * static_cast<int>(gridDim.x);
-    if (warp == kFirst && ptx::lane_id() == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
+    if (warp == kFirstCopyWarp && ptx::lane_id() == 0) stat_min(p, kStatProdStartNs, ptx::globaltimer());
     seed_counters(p, gw, n_gw, true);
     if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
     else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
@@ -912,6 +919,8 @@ __device__ __forceinline__ void embedded_producer(const FusedParams& p)
     seed_counters(p, gw, n_gw, false);
     __syncwarp();
     if (ptx::lane_id() == 0) stat_max(p, kStatProdEndNs, ptx::globaltimer());
+    // the prologue's cluster barrier completes before the teardown's
+    if (PAIR == 2) ptx::cluster_wait();
 }
 
 template <int PAIR, bool DYN, bool EMB>
@@ -920,6 +929,13 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     using T = Tile<PAIR>;
     const int warp = threadIdx.x / 32;
     const ConsumerSmem<PAIR> s = consumer_smem<PAIR>(smem);
+    if (EMB && warp >= kFirstCopyWarp) {
+        embedded_producer<PAIR>(p);
+        // the teardown barrier: TMEM is freed after every warp is done
+        if (PAIR == 1) ptx::bar_sync_unaligned(0, kThreads);
+        else ptx::cluster_sync();
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < T::kStages; ++i) {
             ptx::mbar_init(&s.full[i], 1);
@@ -950,9 +966,10 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     }
     ptx::tc_fence_before();
     // barriers initialised and TMEM allocated in both CTAs before any
-    // cross-CTA arrival or load
-    if (PAIR == 1) __syncthreads();
-    else ptx::cluster_sync();
+    // cross-CTA arrival or load (copy warps only arrive)
+    if (PAIR == 2) ptx::cluster_sync();
+    else if (EMB) ptx::bar_sync_unaligned(1, kFirstCopyWarp * 32);
+    else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
     // the prologue above overlaps the previous kernel; the schedule (a
@@ -971,15 +988,15 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
-        else if (EMB && warp > kGateWarp) embedded_producer(p);
     }
     __syncwarp();
 
     // teardown: every role of both CTAs has finished before TMEM is freed
     // (and before a CTA whose shared memory the peer reads exits)
     ptx::tc_fence_before();
-    if (PAIR == 1) __syncthreads();
-    else ptx::cluster_sync();
+    if (PAIR == 2) ptx::cluster_sync();
+    else if (EMB) ptx::bar_sync_unaligned(0, kThreads);
+    else __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
         if (PAIR == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);

@@ -344,6 +344,25 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for threads that count toward a cluster
+// barrier but have nothing to wait for until later.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// CTA barrier `id` over `n` threads (a multiple of 32), reached from
+// different places in the code by different warps (the non-.aligned form).
+__device__ __forceinline__ void bar_sync_unaligned(int id, int n)
+{
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
