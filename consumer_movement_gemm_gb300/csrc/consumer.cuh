@@ -29,18 +29,18 @@
 
 namespace tovl {
 
-template <int PAIR>
+template <int PAIR, int ST = stages_for(PAIR)>
 struct Tile {
-    static constexpr int kStages = stages_for(PAIR);
+    static constexpr int kStages = ST;
     static constexpr int kStageA = kTileM * kTileK * 2;               // 16 KB
     static constexpr int kStageB = kTileK * kTileN * 2 / PAIR;        // this CTA's B columns
     static constexpr int kStageBytes = kStageA + kStageB;
     static constexpr int kBBoxes = kTileN / 64 / PAIR;                // 64-column TMA boxes per stage
     // M = 128 * PAIR, N = 256, A K-major, B MN-major (W is [K][N], N contiguous)
     static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM * PAIR, kTileN, false, true);
-    static_assert(kStages * kStageBytes + kEpiWarps * kEpiBufBytes + 1024 <= smem_bytes(PAIR),
+    static_assert(kStages * kStageBytes + kEpiWarps * kEpiBufBytes + 1024 <= smem_for(PAIR, ST),
                   "stages and epilogue buffers must fit the dynamic shared memory");
-    static_assert(smem_bytes(PAIR) <= 227 * 1024, "at most 227 KB of shared memory per CTA");
+    static_assert(smem_for(PAIR, ST) <= 227 * 1024, "at most 227 KB of shared memory per CTA");
 };
 
 template <int PAIR>
@@ -62,10 +62,10 @@ struct ConsumerSmem {
 
 constexpr int kRing = 8;
 
-template <int PAIR>
+template <int PAIR, int ST = stages_for(PAIR)>
 __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
 {
-    using T = Tile<PAIR>;
+    using T = Tile<PAIR, ST>;
     ConsumerSmem<PAIR> s;
     s.a = smem;
     s.b = smem + T::kStages * T::kStageA;
@@ -190,11 +190,11 @@ __device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR
 }
 
 // Arm the cursor's stage and issue its B boxes (the stage must be free).
-template <int PAIR>
+template <int PAIR, int ST>
 __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                         BCursor<PAIR>& b)
 {
-    using T = Tile<PAIR>;
+    using T = Tile<PAIR, ST>;
     uint8_t* bdst = s.b + b.stage * T::kStageB;
     if (PAIR == 1) {
         ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
@@ -224,7 +224,7 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
 
 // Arm stages until the cursor is `ahead` stages past `a_count` (blocking on
 // free stages only when `block`).  Returns false on a pipeline timeout.
-template <int PAIR>
+template <int PAIR, int ST>
 __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                       BCursor<PAIR>& b, int upto, bool block)
 {
@@ -234,22 +234,22 @@ __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<P
         } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
             return true;
         }
-        b_issue<PAIR>(p, s, sc, b);
+        b_issue<PAIR, ST>(p, s, sc, b);
     }
     return true;
 }
 
 // TMA lane: wait until the gate warp has passed gate number `idx` (bounded),
 // arming free stages with B meanwhile.
-template <int PAIR>
+template <int PAIR, int ST>
 __device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                           BCursor<PAIR>& b, int a_count, int idx)
 {
-    using T = Tile<PAIR>;
+    using T = Tile<PAIR, ST>;
     if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
     const uint64_t start = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (!b_run<PAIR>(p, s, sc, b, a_count + T::kStages, false)) return false;
+        if (!b_run<PAIR, ST>(p, s, sc, b, a_count + T::kStages, false)) return false;
         if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
         if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
             record_error(p.ctrl, kErrTimeout);
@@ -262,10 +262,10 @@ __device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSm
 // TMA warp: per tile and K-slice, wait for the slice's gate, then stream the
 // slice's A k-blocks into stages whose B the cursor above has already
 // loaded.  One lane issues everything.
-template <int PAIR>
+template <int PAIR, int ST>
 __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
 {
-    using T = Tile<PAIR>;
+    using T = Tile<PAIR, ST>;
     if (ptx::lane_id() != 0) return;
     BCursor<PAIR> b;
     b.t = sc.unit;
@@ -281,7 +281,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
         const int arow = sc.a_row(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
-                if (!wait_gate<PAIR>(p, s, sc, b, a_count, gate_idx)) return;
+                if (!wait_gate<PAIR, ST>(p, s, sc, b, a_count, gate_idx)) return;
                 // the rows were written through the generic proxy; order them
                 // before this thread's tensor-memory-access (async proxy) reads
                 ptx::fence_proxy_async_global();
@@ -289,7 +289,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
             const int kb1 = kb_begin(p, sl + 1);
             for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
                 // this k-block's stage is armed and holds (or receives) its B
-                if (!b_run<PAIR>(p, s, sc, b, a_count + 1, true)) return;
+                if (!b_run<PAIR, ST>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
                 if (PAIR == 1) {
                     ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow);
@@ -305,11 +305,11 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
 }
 
 // MMA warp: one lane (of the pair's first CTA) issues the MMAs.
-template <int PAIR>
+template <int PAIR, int ST>
 __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                              uint32_t tmem_base)
 {
-    using T = Tile<PAIR>;
+    using T = Tile<PAIR, ST>;
     if (ptx::lane_id() != 0 || sc.rank != 0) return;
     uint32_t stage = 0, phase = 0;
     int local = 0;
@@ -934,9 +934,10 @@ __device__ __forceinline__ void embedded_producer(const FusedParams& p)
 template <int PAIR, bool DYN, bool EMB>
 __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 {
-    using T = Tile<PAIR>;
+    constexpr int ST = EMB ? emb_stages_for(PAIR) : stages_for(PAIR);
+    using T = Tile<PAIR, ST>;
     const int warp = threadIdx.x / 32;
-    const ConsumerSmem<PAIR> s = consumer_smem<PAIR>(smem);
+    const ConsumerSmem<PAIR> s = consumer_smem<PAIR, ST>(smem);
     if (EMB && warp >= kFirstCopyWarp) {
         embedded_producer<PAIR>(p);
         // the teardown barrier: TMEM is freed after every warp is done
@@ -992,8 +993,8 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else if (warp < kEpiWarp0 + kEpiWarps) dyn::consumer_epilogue<PAIR, true>(p, s, sc, tmem_base);
         else if (warp == kGateWarp) dyn::consumer_gate<PAIR, true>(p, s, sc);
     } else {
-        if (warp == 0) consumer_tma<PAIR>(p, s, sc);
-        else if (warp == 1) consumer_mma<PAIR>(p, s, sc, tmem_base);
+        if (warp == 0) consumer_tma<PAIR, ST>(p, s, sc);
+        else if (warp == 1) consumer_mma<PAIR, ST>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
     }

@@ -46,10 +46,17 @@ constexpr int kPairStages = 5;                     // pipeline stages of a CTA-p
 // memory is one its loads cannot have in flight, so the stages are as few as
 // keep the tensor pipe fed.
 constexpr int stages_for(int pair) { return pair == 1 ? kStages : kPairStages; }
-constexpr int smem_bytes(int pair)
+constexpr int smem_for(int pair, int stages)
 {
-    return stages_for(pair) * (kStageA + kStageB / pair) + kEpiWarps * kEpiBufBytes + 1024 + 1024;
+    return stages * (kStageA + kStageB / pair) + kEpiWarps * kEpiBufBytes + 1024 + 1024;
 }
+constexpr int smem_bytes(int pair) { return smem_for(pair, stages_for(pair)); }
+// Launches without producer CTAs (embedded producers) leave no SM's L1 to
+// protect: CTA pairs take a sixth stage there (measured: the uniform and Zipf
+// dispatch rounds 2.5-3 % faster; with producer CTAs it cost the TP call 2 us).
+constexpr int kEmbPairStages = 6;
+constexpr int emb_stages_for(int pair) { return pair == 2 ? kEmbPairStages : stages_for(pair); }
+constexpr int smem_bytes_emb(int pair) { return smem_for(pair, emb_stages_for(pair)); }
 
 // Device status codes (mirror tovl.h).
 enum : int {

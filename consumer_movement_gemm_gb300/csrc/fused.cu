@@ -58,7 +58,7 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(grid);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = smem_bytes(pair);
+    lc.dynamicSmemBytes = p.embedded ? smem_bytes_emb(pair) : smem_bytes(pair);
     lc.stream = stream;
     cudaLaunchAttribute attr[3];
     int n = 0;
@@ -100,9 +100,9 @@ cudaError_t prepare_fused()
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fused_kernel<2, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(1));
+        e = cudaFuncSetAttribute(fused_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_emb(1));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fused_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(2));
+        e = cudaFuncSetAttribute(fused_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_emb(2));
     return e;
 }
 
