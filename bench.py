@@ -433,7 +433,7 @@ def dispatch_bench(cfg, rounds: int, dev, producers: int, k_slices: int, align: 
         counts = np.bincount(topk_np.reshape(-1), minlength=cfg.E)
         m_pad = int(offs[-1].item())
         flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.N
-        res = {"workload": cfg.name, "segment_alignment": align, "pair_tiles": bool(h.get_option(tovl.OPT_PAIRS)) and align == 256,
+        res = {"workload": cfg.name, "segment_alignment": align, "pair_tiles": bool(h.get_option(tovl.OPT_PAIRS)) and (align == 256 or bool(h.get_option(tovl.OPT_EMBEDDED))),
                "producer_ctas": h.get_option(tovl.OPT_PRODUCERS),
                "embedded_producers": bool(h.get_option(tovl.OPT_EMBEDDED)), "ms_per_round": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
                "algorithmic_GFLOP": flops / 1e9, "padded_rows": m_pad, "max_expert_rows": int(counts.max()),

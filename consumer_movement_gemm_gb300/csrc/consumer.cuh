@@ -98,9 +98,25 @@ struct Schedule {
         return p.mode == kModeReduceScatter ? t / p.n_shards : t;
     }
     __device__ int shard(const FusedParams& p, int t) const { return p.mode == kModeReduceScatter ? t % p.n_shards : 0; }
+    // 128-row dispatch segments on CTA pairs: tile row r is the plan's pair
+    // tile r (its first block and the next); the next block is a phantom
+    // when it lies past the segment: computed with the segment's weights,
+    // never gated and never stored
+    __device__ int pair_entry(const FusedParams& p, int t) const { return p.pair_tab[1 + out_tile(p, t) / p.n_nb]; }
     __device__ int row_block(const FusedParams& p, int t) const
     {
+        if (PAIR == 2 && p.pair_tab) return (pair_entry(p, t) >> 1) + static_cast<int>(rank);
         return (out_tile(p, t) / p.n_nb) * PAIR + static_cast<int>(rank);
+    }
+    // the row block whose expert's weights the tile multiplies (the pair's first)
+    __device__ int expert_block(const FusedParams& p, int t) const
+    {
+        if (PAIR == 2 && p.pair_tab) return pair_entry(p, t) >> 1;
+        return (out_tile(p, t) / p.n_nb) * PAIR;
+    }
+    __device__ bool phantom(const FusedParams& p, int t) const
+    {
+        return PAIR == 2 && p.pair_tab && rank == 1 && (pair_entry(p, t) & 1) == 0;
     }
     __device__ int col_block(const FusedParams& p, int t) const { return out_tile(p, t) % p.n_nb; }
     // first row of this CTA's part of the tile in the A and output tensors
@@ -119,6 +135,7 @@ __device__ __forceinline__ Schedule<PAIR> make_schedule(const FusedParams& p, in
     sc.unit = cid / PAIR;
     sc.n_units = p.n_consumers / PAIR;
     sc.n_tiles = (num_row_blocks(p) + PAIR - 1) / PAIR * p.n_nb * (p.mode == kModeReduceScatter ? p.n_shards : 1);
+    if (PAIR == 2 && p.pair_tab) sc.n_tiles = p.pair_tab[0] * p.n_nb;
     return sc;
 }
 
@@ -155,8 +172,9 @@ __device__ void consumer_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s,
     int passed = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
         const int mb = sc.row_block(p, t);
+        const bool phantom = sc.phantom(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl) {
-            polls += gate(p, mb, sl);
+            if (!phantom) polls += gate(p, mb, sl);
             ++passed;
             if (lane == 0) {
                 ptx::st_release_cta_smem(s.gates_passed, passed);
@@ -183,7 +201,7 @@ template <int PAIR>
 __device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR>& sc, BCursor<PAIR>& b)
 {
     if (b.t >= sc.n_tiles) return;
-    const int mb = sc.row_block(p, b.t);
+    const int mb = sc.expert_block(p, b.t);
     b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
            : (p.mode == kModeReduceScatter) ? sc.shard(p, b.t) * p.K : 0;
     b.n0 = sc.col_block(p, b.t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
@@ -385,6 +403,14 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             const long long idx = static_cast<long long>(p.trace_tiles) * (p.k_slices + 1) + t;
             if (idx < p.ctrl.trace_cap)
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
+        }
+        if (sc.phantom(p, t)) {
+            // a phantom half (rows past the segment): nothing is stored;
+            // the accumulator goes straight back to the MMA warp
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
+            continue;
         }
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
 #pragma unroll 1

@@ -108,6 +108,11 @@ struct Plan {
     int* pad;             // [block cap] padding rows per block (counter seed)
     int* blk_expert;      // [block cap]
     int* meta;            // [4] m_pad, n_blocks, zero_padding, error
+    // CTA-pair row tiles over 128-row segments: [0] = their count, then per
+    // tile 2 * (first block) + 1 if the next block is in the same segment
+    // (else the pair's second CTA computes a phantom half that is never
+    // stored); null when not wanted
+    int* pair_tab;        // [1 + block cap]
 };
 
 enum : int { kModeGather = 0, kModeDispatch = 1, kModeReduceScatter = 2 };
@@ -143,6 +148,7 @@ struct FusedParams {
     const void* x;
     const int* src_of_dst;
     const int* pad;
+    const int* pair_tab;  // Plan::pair_tab when CTA pairs run 128-row dispatch segments, else null
     const int* blk_expert;
     const int* meta;
     // combine sources (gather mode with a row table)

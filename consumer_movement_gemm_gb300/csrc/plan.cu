@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
     int* s_cnt = sm + p.E + 1;      // [E]
     int* s_seg = sm + 2 * p.E + 1;  // [n_seg][E] segment bases, when they fit
     const bool seg_in_smem = p.n_seg * p.E <= kSegSmemInts;
+    int* s_pb = s_seg + (seg_in_smem ? p.n_seg * p.E : 0);   // [E+1] first pair tile of each segment
     int* seg_base = seg_in_smem ? s_seg : p.plan.seg_count;
     __shared__ int s_zero;
     __shared__ int s_bad;
@@ -143,6 +144,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
             s_off[e + 1] = run;
         }
         if (run > p.row_cap || run / kBlockRows > p.block_cap) s_bad = 1;
+        // pair tiles: ceil(blocks / 2) per segment
+        int pb = 0;
+        for (int e = 0; e < p.E; ++e) {
+            s_pb[e] = pb;
+            pb += ((s_off[e + 1] - s_off[e]) / kBlockRows + 1) / 2;
+        }
+        s_pb[p.E] = pb;
     }
     __syncthreads();
     if (tid <= p.E && prev != s_off[tid]) s_zero = 1;     // benign race: every writer stores 1
@@ -156,6 +164,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
             p.plan.meta[1] = 0;
             p.plan.meta[2] = 0;
             p.plan.meta[3] = 0;
+            if (p.plan.pair_tab) p.plan.pair_tab[0] = 0;
         }
         for (int e = tid; e <= p.E; e += kPlanThreads) p.expert_offsets[e] = 0;
         return;
@@ -171,6 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         p.plan.meta[1] = m_pad / kBlockRows;
         p.plan.meta[2] = s_zero;
         p.plan.meta[3] = 0;
+        if (p.plan.pair_tab) p.plan.pair_tab[0] = s_pb[p.E];
     }
     // destination row of every pair and the inverse map, kDstBatch pairs per
     // thread at a time: the routing and in-segment ranks are loaded together
@@ -201,6 +211,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_finalize_kernel(const PlanP
         p.plan.blk_expert[b] = e;
         const int real = min(max(s_cnt[e] - (b * kBlockRows - s_off[e]), 0), kBlockRows);
         p.plan.pad[b] = kBlockRows - real;
+        const int rel = b - s_off[e] / kBlockRows;
+        if (p.plan.pair_tab && (rel & 1) == 0)
+            p.plan.pair_tab[1 + s_pb[e] + rel / 2] = 2 * b + ((b + 1) * kBlockRows < s_off[e + 1] ? 1 : 0);
     }
     // padding rows (fewer than `align` per expert) have no source token
     for (int x = tid; x < p.E * p.align; x += kPlanThreads) {
@@ -220,7 +233,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream, bool pdl)
 {
     const size_t sm_count = static_cast<size_t>(kPlanWarps) * p.E * sizeof(int);
     const size_t seg = static_cast<size_t>(p.n_seg) * p.E;
-    const size_t sm_fin = (2 * static_cast<size_t>(p.E) + 1 + (seg <= kSegSmemInts ? seg : 0)) * sizeof(int);
+    const size_t sm_fin = (3 * static_cast<size_t>(p.E) + 2 + (seg <= kSegSmemInts ? seg : 0)) * sizeof(int);
     if (p.n_seg > 0) {
         plan_count_kernel<<<p.n_seg, kPlanThreads, sm_count, stream>>>(p);
         const cudaError_t e = cudaGetLastError();

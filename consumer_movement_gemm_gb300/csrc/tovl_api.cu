@@ -175,6 +175,7 @@ static void carve_plan(Carve& c, Plan& p, int E, int max_seg, int max_pairs, lon
     p.pad = c.take<int>(n_blocks);
     p.blk_expert = c.take<int>(n_blocks);
     p.meta = c.take<int>(4);
+    p.pair_tab = c.take<int>(static_cast<size_t>(n_blocks) + 1);
 }
 
 TOVL_API int tovl_create(tovl_handle* out, const tovl_config* cfg_in)
@@ -575,8 +576,12 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     const int align = h->dispatch_align;
     const long long rows = tovl_dispatch_rows_aligned(T, k, E, align);
     if (rows > h->cfg.max_rows) return TOVL_ERR_INVALID;
-    // 256-row segments let a CTA pair take two row blocks of one expert
-    const int pair = (align == 2 * kBlockRows && h->pair_mode && h->max_pairs > 0) ? 2 : 1;
+    // 256-row segments let a CTA pair take two row blocks of one expert; with
+    // 128-row segments and embedded producers CTA pairs take the plan's pair
+    // tiles (two blocks of one segment, or one and a phantom half)
+    const bool pair_ok = h->pair_mode && h->max_pairs > 0;
+    const bool pair_tab = pair_ok && align == kBlockRows && h->embedded != 0;
+    const int pair = (pair_ok && (align == 2 * kBlockRows || pair_tab)) ? 2 : 1;
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -642,6 +647,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.src_of_dst = h->plan.src_of_dst;
     p.pad = h->plan.pad;
     p.blk_expert = h->plan.blk_expert;
+    p.pair_tab = pair_tab ? h->plan.pair_tab : nullptr;
     p.meta = h->plan.meta;
     p.gathered = dispatched;
     p.out = out;
@@ -657,7 +663,8 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
         return rc;
     p.seq = static_cast<int>(h->seq + 1);
     p.gate_seq = p.seq + h->fault_gate_offset;
-    p.trace_tiles = static_cast<int>(rows / kTileM / pair * p.n_nb);
+    // (pair tiles over 128-row segments: at most one per block)
+    p.trace_tiles = static_cast<int>(rows / kTileM / (pair_tab ? 1 : pair) * p.n_nb);
     if ((rc = reset_stats(h, s, p.trace_tiles, p.k_slices)) != TOVL_OK) return rc;
     e = launch(h, p, s, true, pair);
     if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");

@@ -578,6 +578,27 @@ def test_dispatch_most_experts():
             _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
 
 
+def test_dispatch_pair_tiles_phantom_half_at_buffer_end():
+    # 128-row segments on CTA pairs (the default): two experts of one row
+    # each fill the whole buffer (rows = m_pad = 256), so every pair tile is
+    # one block and a phantom half, the last one past the end of the buffer;
+    # then experts of 3, 1 and 2 blocks (odd and even block counts)
+    H, N = 128, 256
+    with _handle(k_slices=2) as h:
+        assert h.get_option(tovl.OPT_EMBEDDED) == 1 and h.get_option(tovl.OPT_DISPATCH_ALIGN) == 128
+        cases = [np.array([[0], [1]], dtype=np.int32),
+                 np.concatenate([np.zeros((300, 1)), np.ones((100, 1)), np.full((200, 1), 2)]).astype(np.int32)]
+        for r, topk_np in enumerate(cases, start=1):
+            T, k = topk_np.shape
+            E = int(topk_np.max()) + 1
+            assert r > 1 or tovl.dispatch_rows(T, k, E) == 256
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 990 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 995 + r, DEV)
+            dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+            assert h.sync_status() == 0
+            _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
+
+
 @pytest.mark.parametrize("routing", list(ROUTINGS))
 @pytest.mark.parametrize("align", [128, 256])
 def test_dispatch_embedded_producers(routing, align):
