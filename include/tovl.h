@@ -308,15 +308,20 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * defines) or 256 (segments padded to two blocks, so CTA pairs compute
  * 256-row tiles inside one expert; the padded rows are zero and their
  * block counters are seeded like any padding; buffers then need
- * tovl_dispatch_rows_aligned(T, k, E, 256) rows),
+ * tovl_dispatch_rows_aligned(T, k, E, 256) rows; with embedded producers
+ * CTA pairs run 128-row segments as well, two blocks of a segment per pair
+ * tile, a segment's odd last block beside a phantom half that is computed
+ * but never stored, so 256 no longer buys speed there),
  * 18 = embedded producers (1, the default: in tovl_dispatch_grouped_gemm;
  * 2 = also in tovl_gather_gemm; 0 = off): the call launches no producer
  * CTAs; every SM (every co-resident CTA pair) is a consumer and the
  * consumer CTAs' five spare warps copy the rows, in the producers' order and
  * with their counters and seeds (16-byte vector copies whatever option 14
- * says; the role switch does not apply).  Measured on GB300: dispatch 6-9 %
- * faster (a wave fewer of expert tiles), the TP gather 6 % slower (its three
- * tile waves stay three; the copy warps share the SMs),
+ * says; the role switch does not apply; CTA pairs on 128-row segments, see
+ * 17).  Measured on GB300: dispatch calls 16-17 % shorter than with
+ * producer CTAs and single-CTA tiles (uniform 141.5 -> 118 us, Zipf 793 ->
+ * 670 us), the TP gather 4-6 % slower (its three tile waves
+ * stay three; the copy warps share the SMs),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in
