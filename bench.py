@@ -461,6 +461,7 @@ def combine_bench(h, cfg, y, timer, rounds: int, dev):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"ms_per_round": ms, "GB/s": gbs, "algorithmic_MB": nbytes / 1e6, "frac_of_hbm": gbs / peaks["hbm_gbs"],
             "producer_ctas": h.get_option(1), "reducer_ctas": h.get_option(2),
+            "copy": "10 copy warps in every CTA, the other 6 reduce" if h.get_option(1) == 0 else "producer CTAs beside reducer CTAs",
             "l2": "flushed before every call (expert outputs start in HBM)"}
 
 

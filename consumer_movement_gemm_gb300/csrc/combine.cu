@@ -14,8 +14,26 @@ __global__ void __launch_bounds__(kThreads, 1) combine_kernel(const __grid_const
     uint8_t* smem = align1024(smem_raw);
     // the expert outputs and the plan come from the kernels before this one
     ptx::grid_dep_wait();
+    if (p.embedded > 0) {
+        // every CTA copies in its first p.embedded warps and reduces in the
+        // rest; copy items and tokens are dealt across all CTAs
+        const int warp = threadIdx.x / 32;
+        const int grid = static_cast<int>(gridDim.x);
+        if (warp < p.embedded) {
+            const int gw = warp * grid + static_cast<int>(blockIdx.x);
+            const int n_gw = p.embedded * grid;
+            seed_counters(p, gw, n_gw, true);
+            if (p.item_rows <= 16) copy_items<1>(p, gw, n_gw);
+            else if (p.item_rows == 32) copy_items<2>(p, gw, n_gw);
+            else copy_items<4>(p, gw, n_gw);
+            seed_counters(p, gw, n_gw, false);
+        } else {
+            reducer(p, static_cast<int>(blockIdx.x), grid, p.embedded);
+        }
+        return;
+    }
     if (static_cast<int>(blockIdx.x) < p.n_producers) producer(p, smem, blockIdx.x);
-    else reducer(p, blockIdx.x - p.n_producers);
+    else reducer(p, blockIdx.x - p.n_producers, p.n_reducers, 0);
 }
 
 // Shared memory: the staged producer path keeps one 8 KB buffer and one

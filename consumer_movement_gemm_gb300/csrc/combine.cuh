@@ -21,18 +21,20 @@ namespace tovl {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ inline void reducer(const FusedParams& p, int rid)
+// Reducer warps first_warp .. 15 of reducer unit `rid` of `n_units` (a
+// reducer CTA, or every CTA when the copy runs in its other warps).
+__device__ inline void reducer(const FusedParams& p, int rid, int n_units, int first_warp)
 {
     const int warp = threadIdx.x / 32;
     const int lane = static_cast<int>(ptx::lane_id());
     if (gather_rows(p) == 0) {
         // the routing plan of the round was rejected: nothing to combine
-        if (rid == 0 && threadIdx.x == 0) record_error(p.ctrl, kErrInvalid);
+        if (rid == 0 && warp == first_warp && lane == 0) record_error(p.ctrl, kErrInvalid);
         return;
     }
     // consecutive tokens go to different CTAs, in the producers' order
-    const int gw = warp * p.n_reducers + rid;
-    const int n_gw = p.n_reducers * (kThreads / 32);
+    const int gw = (warp - first_warp) * n_units + rid;
+    const int n_gw = n_units * (kThreads / 32 - first_warp);
     const int S = p.ctrl.n_slices;
     const int groups = p.N / 8;   // 16-byte column groups of a row
     const size_t row_bytes = static_cast<size_t>(p.N) * 2;

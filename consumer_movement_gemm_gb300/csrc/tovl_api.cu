@@ -791,7 +791,14 @@ TOVL_API int tovl_combine(tovl_handle h, const void* y, int N, const float* gate
     if (P > h->num_sms - 1) P = h->num_sms - 1;
     p.n_producers = P;
     p.n_reducers = h->num_sms - P;
-    h->last_P = P;
+    // embedded copy (option 18, unless a producer count is set): every CTA
+    // copies in its first kCombineCopyWarps warps and reduces in the others
+    if (h->embedded != 0 && h->producers <= 0) {
+        p.n_producers = 0;
+        p.n_reducers = h->num_sms;
+        p.embedded = kCombineCopyWarps;
+    }
+    h->last_P = p.n_producers;
     h->last_C = p.n_reducers;
     p.k_slices = 1;
     {

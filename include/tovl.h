@@ -186,8 +186,10 @@ int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shards, int M
  * the round is a no-op that sets TOVL_ERR_INVALID in the status word; after
  * a dispatch round without tokens (T = 0) the call returns TOVL_OK and does
  * nothing (no round).  Otherwise one round (one sequence number), like the
- * other calls.  Option 1 (producer CTAs) applies; the remaining SMs reduce
- * (default: 7/12 of the SMs copy). */
+ * other calls.  With option 18 on (the default) and no producer count set,
+ * every CTA copies in 10 of its 16 warps and reduces in the other 6;
+ * otherwise producer CTAs copy (option 1, default 7/12 of the SMs) and the
+ * remaining SMs reduce. */
 int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void* staging, void* combined,
                  void* stream);
 
@@ -312,7 +314,8 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * CTA pairs run 128-row segments as well, two blocks of a segment per pair
  * tile, a segment's odd last block beside a phantom half that is computed
  * but never stored, so 256 no longer buys speed there),
- * 18 = embedded producers (1, the default: in tovl_dispatch_grouped_gemm;
+ * 18 = embedded producers (1, the default: in tovl_dispatch_grouped_gemm and
+ * tovl_combine;
  * 2 = also in tovl_gather_gemm; 0 = off): the call launches no producer
  * CTAs; every SM (every co-resident CTA pair) is a consumer and the
  * consumer CTAs' five spare warps copy the rows, in the producers' order and

@@ -289,13 +289,16 @@ def _combine_round(h, rows, N, T, k, seed):
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
-@pytest.mark.parametrize("mode,pdl", [(0, 1), (1, 1), (0, 0)])
-def test_combine_after_dispatch(routing, mode, pdl):
+@pytest.mark.parametrize("mode,pdl,emb", [(0, 1, 1), (0, 0, 1), (0, 1, 0), (1, 1, 0)])
+def test_combine_after_dispatch(routing, mode, pdl, emb):
     # combine runs on a seeded expert-output tensor, so staging and combined
     # rows are compared bit for bit with the oracle's; plan -> fused kernel ->
-    # combine run with and without programmatic dependent launches
+    # combine run with and without programmatic dependent launches; emb 1 (the
+    # default): every CTA copies and reduces, 0: producer and reducer CTAs
+    # (vector or staged copies)
     H, N = 128, 320
     with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_EMBEDDED, emb)
         h.set_option(tovl.OPT_PRODUCER_MODE, mode)
         h.set_option(tovl.OPT_PDL, pdl)
         assert h.get_option(tovl.OPT_PDL) == pdl
