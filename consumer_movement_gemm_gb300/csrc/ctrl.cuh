@@ -55,11 +55,6 @@ constexpr int smem_bytes(int pair) { return smem_for(pair, stages_for(pair)); }
 // protect: CTA pairs take a sixth stage there (measured: the uniform and Zipf
 // dispatch rounds 2.5-3 % faster; with producer CTAs it cost the TP call 2 us).
 constexpr int kEmbPairStages = 6;
-// Combine with embedded copies: copy warps per CTA (the other warps reduce).
-// Measured on GB300 against 88 producer CTAs and 64 reducer CTAs: uniform
-// top-2 26.6 -> 24.7 us, Zipf top-4 72.3 -> 67.4 us; 6, 8, 11, 12 and 13 copy
-// warps slower.
-constexpr int kCombineCopyWarps = 10;
 constexpr int emb_stages_for(int pair) { return pair == 2 ? kEmbPairStages : stages_for(pair); }
 constexpr int smem_bytes_emb(int pair) { return smem_for(pair, emb_stages_for(pair)); }
 
