@@ -42,9 +42,16 @@ __device__ inline void reducer(const FusedParams& p, int rid, int n_units, int f
     uint8_t* out = static_cast<uint8_t*>(p.combined);
     for (int t = gw; t < p.T; t += n_gw) {
         const int s0 = t * p.k;
+        // every chunk that holds one of the token's k staged rows: one or two
+        // for k <= 65, more for larger k (lane i watches chunk c0 + i, 32
+        // chunks per pass)
         const int c0 = s0 / kChunkRows, c1 = (s0 + p.k - 1) / kChunkRows;
-        const int* words[2] = {p.ctrl.slot + c0 * S, p.ctrl.slot + c1 * S};
-        if (warp_wait_ge(words, c1 != c0 ? 2 : 1, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
+        for (int cb = c0; cb <= c1; cb += 32) {
+            const int c = cb + lane;
+            if (warp_wait_lanes(c <= c1 ? p.ctrl.slot + c * S : nullptr, p.gate_seq, p.ctrl, p.seq,
+                                p.timeout_ns) < 0)
+                return;
+        }
         // a lane's column groups are lane, lane + 32, ... below N / 8; kBatch
         // of them are loaded together per staged row, so a token costs k
         // round trips per batch instead of one per group (a group past the

@@ -5,8 +5,10 @@ memory (another framework owns the memory budget, a latency-critical loop
 cannot afford cudaMalloc's device-wide synchronisation, a plugin's host owns
 every allocation).  Its scratch is a fixed array inside the library, shared
 by all calls on a device and keeping the previous call's contents.  This
-file is collected last; it checks the entry point, through the C ABI, against
-the plan the regular dispatch entry point computes, on two calls in a row.
+file is collected last; it checks the entry point, through the C ABI, on two
+calls in a row against the oracle's plan and against the plan the regular
+dispatch entry point computes, and checks that a routing with a bad expert
+id leaves all-zero offsets without spoiling the next call.
 """
 import math
 
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from consumer_movement_gemm_gb300 import tovl
 
@@ -26,9 +29,10 @@ DEV = "cuda"
 def _build():
     from consumer_movement_gemm_gb300 import build
     build.build()
+    oracle.build()
 
 
-def _reference_plan(topk_np, E):
+def _handle_plan(topk_np, E):
     """Expert offsets and destination rows from tovl_dispatch_grouped_gemm."""
     T, k = topk_np.shape
     H, N = 64, 256
@@ -45,22 +49,46 @@ def _reference_plan(topk_np, E):
     return offs.cpu().numpy(), dst
 
 
+def _noalloc(topk_np, E):
+    topk = torch.from_numpy(topk_np).to(DEV)
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+    dst = torch.full((topk_np.size,), -7, dtype=torch.int32, device=DEV)
+    tovl.dispatch_plan_noalloc(topk, E, offs, dst)
+    torch.cuda.synchronize()
+    return offs.cpu().numpy(), dst.cpu().numpy()
+
+
 @pytest.mark.parametrize("routing", ["uniform", "zipf"])
-def test_noalloc_plan_matches_dispatch_plan_twice(routing):
+def test_noalloc_plan_matches_oracle_and_dispatch_plan_twice(routing):
     if routing == "uniform":
         topk_np, E = workloads.uniform_topk(3000, 2, 8, 11), 8
     else:
         topk_np, E = workloads.zipf_topk(8192, 4, 32, 1.2, 12), 32
-    want_off, want_dst = _reference_plan(topk_np, E)
-    topk = torch.from_numpy(topk_np).to(DEV)
+    want = oracle.dispatch_plan(topk_np, E)
+    h_off, h_dst = _handle_plan(topk_np, E)
     for call in range(2):
-        offs = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
-        dst = torch.full((topk_np.size,), -7, dtype=torch.int32, device=DEV)
-        tovl.dispatch_plan_noalloc(topk, E, offs, dst)
-        torch.cuda.synchronize()
+        offs, dst = _noalloc(topk_np, E)
         # integer results: the tolerance is exact equality
-        assert np.array_equal(offs.cpu().numpy(), want_off), f"offsets, call {call}"
-        assert np.array_equal(dst.cpu().numpy(), want_dst), f"destination rows, call {call}"
+        assert np.array_equal(offs, want.off), f"offsets vs oracle, call {call}"
+        assert np.array_equal(dst, want.dst), f"destination rows vs oracle, call {call}"
+        assert np.array_equal(offs, h_off), f"offsets vs the dispatch entry point, call {call}"
+        assert np.array_equal(dst, h_dst), f"destination rows vs the dispatch entry point, call {call}"
+
+
+def test_noalloc_bad_expert_id_gives_zero_offsets_and_next_call_is_clean():
+    # an expert id outside [0, E) makes the plan all-zero offsets; the flag
+    # that records it lives in the shared scratch, so the following valid
+    # call must be cleared of it and agree with the oracle again
+    E = 6
+    bad = workloads.uniform_topk(500, 2, E, 13)
+    bad[123, 1] = E
+    offs, _ = _noalloc(bad, E)
+    assert np.array_equal(offs, np.zeros(E + 1, np.int32))
+    good = workloads.uniform_topk(700, 3, E, 14)
+    want = oracle.dispatch_plan(good, E)
+    offs, dst = _noalloc(good, E)
+    assert np.array_equal(offs, want.off)
+    assert np.array_equal(dst, want.dst)
 
 
 def test_noalloc_plan_rejects_sizes_beyond_its_scratch():

@@ -158,6 +158,13 @@ def gate_weights(T: int, k: int, seed: int) -> np.ndarray:
     return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
+def repeated_topk(T: int, k: int, E: int, seed: int) -> np.ndarray:
+    """k experts per token drawn uniformly WITH replacement (int32 [T][k]):
+    k may exceed E and a token may name one expert several times."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(0, E, size=(T, k), dtype=np.int32)
+
+
 def all_to_one_topk(T: int, E: int, e: int = 0) -> np.ndarray:
     """Degenerate routing: every token to expert e (k = 1)."""
     return np.full((T, 1), e, np.int32)
