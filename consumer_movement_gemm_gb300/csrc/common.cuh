@@ -27,6 +27,13 @@ __device__ __forceinline__ void trace_put(const FusedParams& p, long long idx, u
     if (p.stats && idx < p.ctrl.trace_cap) p.ctrl.trace[idx] = static_cast<long long>(v);
 }
 
+// L2 cache policy of one stream: `last_bit` set -> evict last, `first_bit`
+// set -> evict first, neither -> evict normal (bits of FusedParams::l2_hints).
+__device__ __forceinline__ uint64_t stream_policy(const FusedParams& p, int last_bit, int first_bit)
+{
+    return ptx::l2_policy((p.l2_hints & last_bit) ? 2 : (p.l2_hints & first_bit) ? 1 : 0);
+}
+
 // Number of 128-row blocks the producers fill and the consumers traverse.
 // Rows of a gather-mode round: p.M, or none when the round's row table comes
 // from a routing plan that was rejected.

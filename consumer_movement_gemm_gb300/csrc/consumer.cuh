@@ -195,6 +195,7 @@ struct BCursor {
     int t, kb, brow, n0;      // next k-block to load: tile, k-block, B row base, B column base
     int issued;               // stages armed so far
     uint32_t stage, phase;
+    uint64_t pol;             // L2 policy of the weight loads
 };
 
 template <int PAIR>
@@ -218,15 +219,16 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
         ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
 #pragma unroll
         for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
-                             b.brow + b.kb * kTileK);
+            ptx::tma_load_2d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
+                                  b.brow + b.kb * kTileK, b.pol);
     } else {
         // both CTAs' bytes are counted on the first CTA's barrier
         if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
 #pragma unroll
         for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64, b.brow + b.kb * kTileK);
+            ptx::tma_load_2d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64,
+                                       b.brow + b.kb * kTileK, b.pol);
     }
     ++b.issued;
     if (++b.stage == T::kStages) {
@@ -291,6 +293,8 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     b.issued = 0;
     b.stage = 0;
     b.phase = 0;
+    b.pol = stream_policy(p, kHintBLast, 0);
+    const uint64_t pol_a = stream_policy(p, 0, kHintAFirst);
     b_tile<PAIR>(p, sc, b);
     uint32_t stage = 0;
     int a_count = 0;
@@ -310,10 +314,10 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 if (!b_run<PAIR, ST>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
                 if (PAIR == 1) {
-                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow);
+                    ptx::tma_load_2d_hint(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow, pol_a);
                 } else {
                     const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
-                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, arow);
+                    ptx::tma_load_2d_pair_hint(adst, &p.tmap_a, bar0, kb * kTileK, arow, pol_a);
                 }
                 ++a_count;
                 if (++stage == T::kStages) stage = 0;
@@ -369,6 +373,21 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     }
 }
 
+// Reduce-scatter: publish partial tile t once this warp's bulk store groups
+// other than the newest LEFT are complete (LEFT = 0: all of them).
+template <int PAIR, int LEFT>
+__device__ __forceinline__ void rs_publish(const FusedParams& p, int t, uint32_t lane)
+{
+    if (lane == 0) {
+        ptx::bulk_wait<LEFT>();
+        ptx::fence_proxy_async_global();
+    }
+    __syncwarp();
+    static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
+    if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
+    __syncwarp();
+}
+
 // Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) ->
 // shared memory -> TMA tensor store.  Warp w reads TMEM lane quarter w % 4
 // (the quarter its position allows), i.e. 32 output rows, and one half of
@@ -390,6 +409,9 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
+    const uint64_t pol_out = stream_policy(p, 0, kHintOutFirst);
+    constexpr int kBoxes = kTileN / 2 / kEpiBoxCols;   // TMA store groups per tile and warp
+    int pending = -1;    // reduce-scatter: the tile whose stores are in flight, published one tile later
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const int arow = sc.a_row(p, t);
@@ -445,25 +467,22 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                  arow + q * 32);
+                ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                       arow + q * 32, pol_out);
                 ptx::bulk_commit();
             }
         }
         if (p.mode == kModeReduceScatter) {
-            // Publish the partial tile ("cross-GPU sync protocols on PCIe",
-            // section 3): once this warp's stores have written global memory,
-            // it arrives on the tile's counter with its share of the
-            // 64-unit quota; the arrival that completes the count is elected
-            // and release-stores the sequence into the tile's slot.
-            if (lane == 0) {
-                ptx::bulk_wait<0>();
-                ptx::fence_proxy_async_global();
-            }
-            __syncwarp();
-            static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
-            if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
-            __syncwarp();
+            // Publish the previous partial tile ("cross-GPU sync protocols on
+            // PCIe", section 3): once this warp's stores of it have written
+            // global memory -- every bulk group but this tile's kBoxes is
+            // complete -- it arrives on that tile's counter with its share of
+            // the 64-unit quota; the arrival that completes the count is
+            // elected and release-stores the sequence into the tile's slot.
+            // Publishing one tile late keeps the wait for store completion
+            // off the path from one accumulator drain to the next.
+            if (pending >= 0) rs_publish<PAIR, kBoxes>(p, pending, lane);
+            pending = t;
         }
         if (p.stats && lane == 0) {
             const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
@@ -471,6 +490,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
         }
     }
+    // the last partial tile: all its stores complete, then published
+    if (pending >= 0) rs_publish<PAIR, 0>(p, pending, lane);
     // every store has written global memory before the CTA retires
     if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();
@@ -617,6 +638,7 @@ struct BCursor {
     bool have;                // t is known (a dynamic schedule publishes tiles as it goes)
     int issued;               // stages armed so far
     uint32_t stage, phase;
+    uint64_t pol;             // L2 policy of the weight loads
 };
 
 // Resolve the cursor's tile: 1 = known (t >= n_tiles: no more tiles), 0 = not
@@ -659,15 +681,16 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
         ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
 #pragma unroll
         for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
-                             b.brow + b.kb * kTileK);
+            ptx::tma_load_2d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
+                                  b.brow + b.kb * kTileK, b.pol);
     } else {
         // both CTAs' bytes are counted on the first CTA's barrier
         if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
 #pragma unroll
         for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_pair(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64, b.brow + b.kb * kTileK);
+            ptx::tma_load_2d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64,
+                                       b.brow + b.kb * kTileK, b.pol);
     }
     ++b.issued;
     if (++b.stage == T::kStages) {
@@ -740,6 +763,8 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     b.issued = 0;
     b.stage = 0;
     b.phase = 0;
+    b.pol = stream_policy(p, kHintBLast, 0);
+    const uint64_t pol_a = stream_policy(p, 0, kHintAFirst);
     uint32_t stage = 0;
     int a_count = 0;
     int gate_idx = 0;
@@ -760,10 +785,10 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                 if (!b_run<PAIR, DYN>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
                 if (PAIR == 1) {
-                    ptx::tma_load_2d(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow);
+                    ptx::tma_load_2d_hint(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow, pol_a);
                 } else {
                     const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[stage]), 0);
-                    ptx::tma_load_2d_pair(adst, &p.tmap_a, bar0, kb * kTileK, arow);
+                    ptx::tma_load_2d_pair_hint(adst, &p.tmap_a, bar0, kb * kTileK, arow, pol_a);
                 }
                 ++a_count;
                 if (++stage == T::kStages) stage = 0;
@@ -842,6 +867,7 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
+    const uint64_t pol_out = stream_policy(p, 0, kHintOutFirst);
     for (int local = 0;; ++local) {
         int t;
         if (!__all_sync(0xffffffffu, kth_tile<PAIR, DYN>(p, s, sc, local, t))) break;
@@ -895,8 +921,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                ptx::tma_store_2d(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                  arow + q * 32);
+                ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                       arow + q * 32, pol_out);
                 ptx::bulk_commit();
             }
         }
@@ -1023,6 +1049,15 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else if (warp == 1) consumer_mma<PAIR, ST>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
+        else if (warp >= kGateWarp && p.mode == kModeReduceScatter && p.rs_epi) {
+            // no producer CTAs: the gate warp and the spare warps add the
+            // per-round quota seeds of the counters this round does not fill,
+            // then sum the output tiles this CTA (pair) owns
+            constexpr int kSpare = kThreads / 32 - kGateWarp;
+            seed_counters(p, (warp - kGateWarp) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x),
+                          kSpare * static_cast<int>(gridDim.x), false);
+            rs_reduce_owned(p, sc.unit, sc.n_units, static_cast<int>(sc.rank), kGateWarp);
+        }
     }
     __syncwarp();
 

@@ -232,7 +232,11 @@ __global__ void __launch_bounds__(kCopyThreads, 2) copy_kernel(const __grid_cons
 
 namespace tovl {
 
-cudaError_t launch_copy(const CopyParams& p, int n_waiters, cudaStream_t stream)
+// Waiter CTAs spin on slots the copier CTAs publish, so a gated copy asks
+// for the cooperative co-residency guarantee (unless `cooperative` is off, for
+// tools that cannot replay cooperative launches; the grid is sized to fit the
+// device either way).
+cudaError_t launch_copy(const CopyParams& p, int n_waiters, bool cooperative, cudaStream_t stream)
 {
     const int grid = p.n_copiers + n_waiters;
     cudaLaunchConfig_t lc = {};
@@ -242,7 +246,7 @@ cudaError_t launch_copy(const CopyParams& p, int n_waiters, cudaStream_t stream)
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = n_waiters > 0 ? 1 : 0;
+    attr[0].val.cooperative = (cooperative && n_waiters > 0) ? 1 : 0;
     lc.attrs = attr;
     lc.numAttrs = 1;
     return cudaLaunchKernelEx(&lc, copy_kernel, p);

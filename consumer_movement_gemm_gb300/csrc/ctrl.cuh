@@ -117,6 +117,20 @@ struct Plan {
 
 enum : int { kModeGather = 0, kModeDispatch = 1, kModeReduceScatter = 2 };
 
+// L2 eviction priorities per stream of a fused call (FusedParams::l2_hints):
+// producer source loads evict-last (a dispatch reads a token row k times) or
+// evict-first (read once), producer destination stores evict-last (the GEMM
+// reads them later), A tensor loads evict-first, weight (B) tensor loads
+// evict-last, output tensor stores evict-first (never read in the call).
+enum : int {
+    kHintSrcLast = 1,
+    kHintOutFirst = 2,
+    kHintAFirst = 4,
+    kHintBLast = 8,
+    kHintDstLast = 16,
+    kHintSrcFirst = 32,
+};
+
 struct FusedParams {
     CUtensorMap tmap_a;   // A: gathered / dispatched rows [rows][K] bf16, box 64 x 128, 128B swizzle
     CUtensorMap tmap_b;   // B: weights [(E*)K][N] bf16 row-major (MN-major operand), box 64 x 64
@@ -140,6 +154,7 @@ struct FusedParams {
     int item_rows;        // rows per producer item (a power of two dividing 64)
     int producer_mode;    // 0: vector copies through registers; 1: bulk loads staged in shared memory
     int trace_tiles;      // tile count bound that lays out the timeline (gate times, then end times)
+    int l2_hints;         // L2 eviction priorities of the call's streams (kHint* bits)
     // gather sources
     const void* shard[kMaxShards];
     int n_shards;
@@ -163,6 +178,8 @@ struct FusedParams {
     int rs_tiles;         // partial tiles: S x output tiles; tile t publishes counter t
     int rs_pair;          // rows of an output tile / 128
     int rs_join;          // consumers take reduction items once their tiles are done (role switch)
+    int rs_epi;           // no producer CTAs: output tile o is summed in the epilogue of the CTA (pair)
+                          // that computes shard (o mod S)'s partial of it
     int dyn;              // consumer tiles handed out by a ticket counter (ctrl.work, zeroed by the plan kernel)
     int join;             // producer CTAs become consumers once their copies are done (role switch)
     int embedded;         // no producer CTAs: the consumer CTAs' spare warps copy the rows

@@ -21,7 +21,7 @@ cudaError_t prepare_combine();
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream, bool pdl);
 cudaError_t prepare_plan();
 
-cudaError_t launch_copy(const CopyParams& p, int n_waiters, cudaStream_t stream);
+cudaError_t launch_copy(const CopyParams& p, int n_waiters, bool cooperative, cudaStream_t stream);
 cudaError_t prepare_copy();
 int copy_max_active_per_sm(int copy_mode);
 int copy_bulk_max_row_bytes();

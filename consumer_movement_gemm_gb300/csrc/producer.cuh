@@ -192,7 +192,7 @@ __device__ __forceinline__ ItemState<M> begin_item(const FusedParams& p, const L
 // which makes every load wait for the one before it.
 template <int M>
 __device__ __forceinline__ void load_pass(const ItemState<M>& st, const LaneMap<M>& lm, int ps,
-                                          int4 (&v)[kItemInt4 / 32])
+                                          int4 (&v)[kItemInt4 / 32], uint64_t pol)
 {
     constexpr int QN = kItemInt4 / 32 / M;    // words per row per lane and pass
 #pragma unroll
@@ -200,20 +200,20 @@ __device__ __forceinline__ void load_pass(const ItemState<M>& st, const LaneMap<
         const int m = k / QN, q = k % QN;
         const int c = lm.lo + lm.L * (ps * QN + q);
         const int4* a = reinterpret_cast<const int4*>(st.src[m]) + (c < st.n16 ? c : 0);
-        v[k] = ptx::ld_nc_v4(a);
+        v[k] = ptx::ld_nc_v4_hint(a, pol);
     }
 }
 
 template <int M>
 __device__ __forceinline__ void store_pass(const ItemState<M>& st, const LaneMap<M>& lm, int ps,
-                                           const int4 (&v)[kItemInt4 / 32])
+                                           const int4 (&v)[kItemInt4 / 32], uint64_t pol)
 {
     constexpr int QN = kItemInt4 / 32 / M;
 #pragma unroll
     for (int k = 0; k < kItemInt4 / 32; ++k) {
         const int m = k / QN, q = k % QN;
         const int c = lm.lo + lm.L * (ps * QN + q);
-        if (st.has[m] && c < st.n16) ptx::st_v4(reinterpret_cast<int4*>(st.dst[m]) + c, v[k]);
+        if (st.has[m] && c < st.n16) ptx::st_v4_hint(reinterpret_cast<int4*>(st.dst[m]) + c, v[k], pol);
     }
 }
 
@@ -226,6 +226,8 @@ __device__ void copy_items(const FusedParams& p, int gw, int n_gw)
     const int n_items = n_blocks * p.k_slices * (kBlockRows / p.item_rows);
     // words a lane covers per pass, per row: QN words L apart
     const int per_pass = lm.L * (kItemInt4 / 32 / M);
+    const uint64_t pol_src = stream_policy(p, kHintSrcLast, kHintSrcFirst);
+    const uint64_t pol_dst = stream_policy(p, kHintDstLast, 0);
     // Every item is released as soon as it is copied: a warp's consecutive
     // items are n_gw items apart in the consumers' order, so holding one back
     // to share a release fence would delay an earlier K-slice behind later
@@ -238,8 +240,8 @@ __device__ void copy_items(const FusedParams& p, int gw, int n_gw)
         const int passes = (st.n16 + per_pass - 1) / per_pass;
         for (int ps = 0; ps < passes; ++ps) {
             int4 v[kItemInt4 / 32];
-            load_pass<M>(st, lm, ps, v);
-            store_pass<M>(st, lm, ps, v);
+            load_pass<M>(st, lm, ps, v, pol_src);
+            store_pass<M>(st, lm, ps, v, pol_dst);
         }
         // the copies above happen-before lane 0's release below
         __syncwarp();
@@ -321,7 +323,7 @@ __device__ void copy_items_staged(const FusedParams& p, uint8_t* smem, int gw, i
 // the start, a consumer warp once its CTA's tiles are done (the role switch)
 // -- takes the next one.  For each item the warp waits until the S partial
 // tiles of its output tile are published (lane s polls tile s's slot with
-// acquire loads; warp vote), then sums the S bf16 partials of its rows in
+// acquire loads; warp vote; 32 shards per pass), then sums the S bf16 partials of its rows in
 // fp32, ascending s, and stores the bf16 result, four rows at a time.  Lane l
 // owns the 16-byte column group l of each row (32 groups = 256 columns).
 // Shards are read four at a time, so each lane has 16 loads in flight.
@@ -349,8 +351,11 @@ static __device__ __noinline__ void rs_reduce(const FusedParams& p)
         const int u = i / per_tile;
         const int item_r0 = (u / p.n_nb) * tile_rows + (i - u * per_tile) * kItemRows;
         if (item_r0 >= M) continue;
-        const int* mine = lane < S ? p.ctrl.slot + u * S + lane : nullptr;
-        if (warp_wait_lanes(mine, p.gate_seq, p.ctrl, p.seq, p.timeout_ns) < 0) return;
+        bool ok = true;
+        for (int s0 = 0; s0 < S && ok; s0 += 32)     // lane s polls shard s0 + s (up to 64 shards)
+            ok = warp_wait_lanes(s0 + lane < S ? p.ctrl.slot + u * S + s0 + lane : nullptr, p.gate_seq, p.ctrl, p.seq,
+                                 p.timeout_ns) >= 0;
+        if (!ok) return;
         const size_t col = static_cast<size_t>(u % p.n_nb) * kTileN * 2 + static_cast<size_t>(lane) * 16;
 #pragma unroll 1
         for (int r0 = item_r0; r0 < item_r0 + kItemRows; r0 += kRows) {
@@ -394,6 +399,92 @@ static __device__ __noinline__ void rs_reduce(const FusedParams& p)
                 o.z = static_cast<int>(ptx::pack_bf16x2(acc[j][4], acc[j][5]));
                 o.w = static_cast<int>(ptx::pack_bf16x2(acc[j][6], acc[j][7]));
                 ptx::st_v4(reinterpret_cast<int4*>(dst + j * row_bytes), o);
+            }
+        }
+    }
+}
+
+// Reduce-scatter reduction by the partial tiles' own CTAs (rs_epi).  The CTA
+// (pair) that computes shard (o mod S)'s partial of output tile o also sums
+// that tile, in `n_warps` warps that are otherwise idle in this launch
+// (warps first_warp..15): for each of this CTA's tiles it owns, they wait
+// until all S partials of the tile are published (lane s polls partial tile
+// o*S + s's slot with acquire loads, warp vote, 32 shards per pass), then
+// reduce this CTA's 128 rows x 256 columns of it,
+//   out[m][n] = bf16( sum_s f32(P_s[m][n]) ), fp32 sums in ascending s,
+// reading the partials from global memory, where they were stored
+// microseconds earlier (L2).  A warp takes rows w, w + n_warps, ...; one row
+// of the tile is 32 lanes x 16 bytes, and four rows of four shards are loaded
+// together (16 loads in flight per lane).  The epilogue warps never wait on
+// these warps, so a reduction overlaps the following tiles.
+constexpr int kRsRows = 4;        // rows per batch
+constexpr int kRsShards = 4;      // shards loaded together
+
+static __device__ __noinline__ void rs_reduce_owned(const FusedParams& p, int unit, int n_units, int rank, int first_warp)
+{
+    const int lane = static_cast<int>(ptx::lane_id());
+    const int w = static_cast<int>(threadIdx.x / 32) - first_warp;
+    const int n_warps = kThreads / 32 - first_warp;
+    const int S = p.n_shards;
+    const int n_tiles = p.rs_tiles;
+    const size_t row_bytes = static_cast<size_t>(p.N) * 2;
+    const size_t shard_bytes = static_cast<size_t>(p.M) * row_bytes;
+    for (int t = unit; t < n_tiles; t += n_units) {
+        const int o = t / S;
+        if (t % S != o % S) continue;               // another CTA (pair) owns output tile o
+        for (int s0 = 0; s0 < S; s0 += 32)
+            if (warp_wait_lanes(s0 + lane < S ? p.ctrl.slot + o * S + s0 + lane : nullptr, p.gate_seq, p.ctrl, p.seq,
+                                p.timeout_ns) < 0)
+                return;
+        // this CTA's rows of the tile: row block (o / n_nb) * rs_pair + rank
+        const int row0 = ((o / p.n_nb) * p.rs_pair + rank) * kTileM;
+        const size_t col = static_cast<size_t>(o % p.n_nb) * kTileN * 2 + static_cast<size_t>(lane) * 16;
+        const uint8_t* part = static_cast<const uint8_t*>(p.out) + col;
+        uint8_t* out = static_cast<uint8_t*>(p.rs_out) + col;
+#pragma unroll 1
+        for (int r = w * kRsRows; r < kTileM; r += n_warps * kRsRows) {
+            // rows r .. r + kRsRows - 1 of the CTA's 128 (kTileM is a multiple of kRsRows)
+            float acc[kRsRows][8];
+#pragma unroll
+            for (int j = 0; j < kRsRows; ++j)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[j][c] = 0.0f;
+            const uint8_t* base = part + static_cast<size_t>(row0 + r) * row_bytes;
+#pragma unroll 1
+            for (int sb = 0; sb < S; sb += kRsShards) {
+                int4 v[kRsShards][kRsRows];
+#pragma unroll
+                for (int q = 0; q < kRsShards; ++q) {
+                    // shards past S re-read the last one (unconditional loads; their sums are skipped)
+                    const int sh = min(sb + q, S - 1);
+#pragma unroll
+                    for (int j = 0; j < kRsRows; ++j)
+                        v[q][j] = ptx::ld_v4(reinterpret_cast<const int4*>(base + sh * shard_bytes + j * row_bytes));
+                }
+#pragma unroll
+                for (int q = 0; q < kRsShards; ++q) {
+                    if (sb + q >= S) break;
+#pragma unroll
+                    for (int j = 0; j < kRsRows; ++j) {
+                        const uint32_t u[4] = {static_cast<uint32_t>(v[q][j].x), static_cast<uint32_t>(v[q][j].y),
+                                               static_cast<uint32_t>(v[q][j].z), static_cast<uint32_t>(v[q][j].w)};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            acc[j][2 * c] = __fadd_rn(acc[j][2 * c], __uint_as_float(u[c] << 16));
+                            acc[j][2 * c + 1] = __fadd_rn(acc[j][2 * c + 1], __uint_as_float(u[c] & 0xffff0000u));
+                        }
+                    }
+                }
+            }
+            uint8_t* dst = out + static_cast<size_t>(row0 + r) * row_bytes;
+#pragma unroll
+            for (int j = 0; j < kRsRows; ++j) {
+                int4 o4;
+                o4.x = static_cast<int>(ptx::pack_bf16x2(acc[j][0], acc[j][1]));
+                o4.y = static_cast<int>(ptx::pack_bf16x2(acc[j][2], acc[j][3]));
+                o4.z = static_cast<int>(ptx::pack_bf16x2(acc[j][4], acc[j][5]));
+                o4.w = static_cast<int>(ptx::pack_bf16x2(acc[j][6], acc[j][7]));
+                ptx::st_v4(reinterpret_cast<int4*>(dst + j * row_bytes), o4);
             }
         }
     }

@@ -30,7 +30,7 @@ struct tovl_ctx {
     int producers = 0;       // 0 = automatic split per call
     int last_P = 0, last_C = 0;
     int consumers = 0;
-    int copy_mode = 1;
+    int copy_mode = TOVL_COPY_VECTOR;   // measured >= 71 % of HBM at every row size (bulk: 3-61 % gated)
     int stats = 0;
     long long timeout_ns = 2000000000LL;
     int copy_ctas = 0;       // copy sweep copiers (0 = auto)
@@ -46,6 +46,8 @@ struct tovl_ctx {
     bool pdl = true;           // programmatic dependent launch between this library's kernels
     int role_switch = 1;       // 1: dispatch (single-CTA tiles) and reduce-scatter roles switch; 2: CTA-pair dispatch too
     int embedded = 1;          // without producer CTAs, the consumer CTAs' spare warps copy: 1 dispatch, 2 also gather
+    int rs_epi = 0;            // 1: reduce-scatter tiles are summed by their owners' idle warps (no producer CTAs)
+    int l2_hints = -1;         // kHint* bits for every fused call; -1 = each call's measured default
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
     Ctrl ctrl{};
@@ -88,7 +90,7 @@ TOVL_API void tovl_default_config(tovl_config* cfg, int device)
     cfg->producer_ctas = 0;
     cfg->consumer_ctas = 0;
     cfg->wait_timeout_ns = 0;
-    cfg->copy_mode = 1;
+    cfg->copy_mode = TOVL_COPY_VECTOR;
     cfg->max_rows = 1 << 16;
     cfg->max_pairs = 1 << 16;
     cfg->max_experts = 64;
@@ -329,7 +331,18 @@ static void base_params(tovl_ctx* h, FusedParams& p)
     p.pipe_timeout_ns = pipe_timeout(h);
     p.stats = h->stats;
     p.producer_mode = h->producer_mode;
+    p.l2_hints = h->l2_hints > 0 ? h->l2_hints : 0;
     p.ctrl = h->ctrl;
+}
+
+// A call's L2 eviction hints when the handle leaves them to the call
+// (option 20 = -1).  Measured on GB300 in interleaved A/B runs: weights
+// evict-last shortens the uniform dispatch by 2 us and the Zipf dispatch by
+// 10 us of 670; for the TP gather, shard loads evict-first (read once) with
+// weights evict-last takes 0.9 us off the fused call.
+static void default_hints(const tovl_ctx* h, FusedParams& p, int hints)
+{
+    if (h->l2_hints < 0) p.l2_hints = hints;
 }
 
 // Producer / consumer CTA split for one call.  With no fixed producer count,
@@ -495,6 +508,7 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
         p.embedded = 1;
     }
     call_geometry(h, p, C, split_pair);
+    default_hints(h, p, kHintSrcFirst | kHintBLast);
     p.n_shards = S;
     p.rows_per_shard = R;
     for (int s = 0; s < S; ++s) p.shard[s] = shards ? shards[s] : nullptr;
@@ -643,6 +657,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.join = dyn ? 1 : 0;
     p.embedded = emb ? 1 : 0;
     call_geometry(h, p, C, pair);
+    default_hints(h, p, kHintBLast);
     p.x = x;
     p.src_of_dst = h->plan.src_of_dst;
     p.pad = h->plan.pad;
@@ -715,7 +730,19 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     int P, C;
     split_ctas(h, P, C, n_mb, n_nb * num_shards, 2.0 * (num_shards + 1) * M * N,
                2.0 * num_shards * static_cast<double>(M) * N * Ks, pair);
-    if (h->producers == 0 && h->role_switch) {
+    if (h->producers == 0 && h->rs_epi) {
+        // every SM (co-resident pair) computes partial tiles; the computer of
+        // shard (o mod S)'s partial of output tile o sums that tile's S
+        // partials in its epilogue, from L2, right after they are published
+        C = (pair == 2 && 2 * h->max_pairs < h->num_sms) ? 2 * h->max_pairs : h->num_sms;
+        if (h->consumers > 0 && h->consumers < C) C = h->consumers;
+        if (pair == 2) C &= ~1;
+        P = 0;
+        h->last_P = P;
+        h->last_C = C;
+        p.rs_epi = 1;
+        p.rs_join = 0;
+    } else if (h->producers == 0 && h->role_switch) {
         // the consumers take over the reduction once their tiles are done, so
         // the producers only need to keep pace while the GEMM runs: about a
         // tenth of the SMs (measured on the TP shape: 16 of 152 best)
@@ -749,9 +776,11 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     p.gate_seq = p.seq + h->fault_gate_offset;
     p.trace_tiles = static_cast<int>(tiles);
     if ((rc = reset_stats(h, s, tiles, 1)) != TOVL_OK) return rc;
-    // the reduction items are handed out by a ticket counter that starts at 0
-    cudaError_t e = cudaMemsetAsync(h->ctrl.work, 0, sizeof(int), s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "ticket reset");
+    // the reduction items of producer CTAs are handed out by a ticket
+    // counter that starts at 0 (the epilogue reduction takes no tickets)
+    cudaError_t e = cudaSuccess;
+    if (!p.rs_epi && (e = cudaMemsetAsync(h->ctrl.work, 0, sizeof(int), s)) != cudaSuccess)
+        return cuda_fail(h, e, "ticket reset");
     e = launch(h, p, s, true, pair);
     if (e != cudaSuccess) return cuda_fail(h, e, "reduce-scatter launch");
     h->seq += 1;
@@ -870,7 +899,7 @@ TOVL_API int tovl_gated_copy(tovl_handle h, const void* src, void* dst, long lon
     if (copiers < 1) return TOVL_ERR_INVALID;
     p.n_copiers = copiers;
     p.seq = static_cast<int>(p.gated ? h->seq + 1 : h->seq);
-    const cudaError_t e = launch_copy(p, waiters, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_copy(p, waiters, h->coop_enabled, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "copy launch");
     if (p.gated) h->seq += 1;
     h->last_stream = static_cast<cudaStream_t>(stream);
@@ -1059,6 +1088,14 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value < 0 || value > 2) return TOVL_ERR_INVALID;
         h->embedded = static_cast<int>(value);
         return TOVL_OK;
+    case 19:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->rs_epi = static_cast<int>(value);
+        return TOVL_OK;
+    case 20:
+        if (value < -1 || value > 63) return TOVL_ERR_INVALID;
+        h->l2_hints = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -1086,6 +1123,8 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 16: *value = h->role_switch; return TOVL_OK;
     case 17: *value = h->dispatch_align; return TOVL_OK;
     case 18: *value = h->embedded; return TOVL_OK;
+    case 19: *value = h->rs_epi; return TOVL_OK;
+    case 20: *value = h->l2_hints; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

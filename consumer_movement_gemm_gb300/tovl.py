@@ -42,6 +42,8 @@ OPT_PDL = 15
 OPT_ROLE_SWITCH = 16
 OPT_DISPATCH_ALIGN = 17
 OPT_EMBEDDED = 18
+OPT_RS_EPILOGUE = 19
+OPT_L2_HINTS = 20
 
 
 class TovlError(RuntimeError):

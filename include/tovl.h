@@ -68,7 +68,9 @@ typedef struct {
                                   then grown while the GEMM keeps its wave count */
     int consumer_ctas;         /* C; 0 = all remaining SMs */
     long long wait_timeout_ns; /* bound of every device wait; 0 = 2 s */
-    int copy_mode;             /* tovl_copy_mode of tovl_gated_copy */
+    int copy_mode;             /* tovl_copy_mode of tovl_gated_copy; the default is
+                                  TOVL_COPY_VECTOR (measured on GB300: 71-91 % of the
+                                  HBM copy bandwidth gated, 256 B to 16 KB rows) */
     long long max_rows;        /* capacity in rows of gathered/dispatched buffers and copies */
     int max_pairs;             /* largest T*k of a dispatch call */
     int max_experts;           /* largest E of a dispatch call (<= 512) */
@@ -150,16 +152,18 @@ int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int H, const
  * is published with the single-writer protocol: its epilogue warps arrive on
  * the tile's counter (acq_rel) once their stores are in global memory, and
  * the last arrival release-stores the sequence into the tile's slot.  The
- * producer CTAs poll the S slots of an output tile (acquire) and write
+ * reducers poll the S slots of an output tile (acquire) and write
  *   out[m][n] = bf16( sum_s f32(P_s[m][n]) ), fp32 sums in ascending s.
+ * By default producer CTAs reduce; with option 19 = 1 (and no producer count
+ * set) the reducer of output tile o is the CTA pair that computes shard
+ * (o mod S)'s partial of it.
  *   X           device, bf16 [S][M][Ks]
  *   num_shards  S, 1..64
  *   M           rows, a multiple of 128
  *   Ks          multiple of 64, at most 32768
  *   W           device, bf16 [S][Ks][N], N a multiple of 256
  *   partials    device, bf16 [S][M][N]: receives P_s
- *   out         device, bf16 [M][N]: receives the reduced rows (shard r owns
- *               rows [r*M/S, (r+1)*M/S) when S divides M)
+ *   out         device, bf16 [M][N]: receives the reduced rows
  * Partial tiles (S x (M/128) x (N/256), or half that with CTA pairs) must
  * not exceed max_rows/64 x k_slices, the handle's counter capacity.  One
  * round (one sequence number). */
@@ -207,15 +211,20 @@ int tovl_combine(tovl_handle h, const void* y, int N, const float* gate_w, void*
  * library until the process exits).
  *   topk_idx        device, int32 [T][k], expert of each pair in [0, E)
  *   expert_offsets  device, int32 [E+1]: padded segment starts (multiples of
- *                   128); all zero if an expert id is out of range
+ *                   128); all zero if an expert id is out of range (the only
+ *                   report of that error: this entry point has no status word)
  *   dst_rows        device, int32 [T*k]: destination row of each pair, rows
- *                   of one expert in ascending (t, j) order
+ *                   of one expert in ascending (t, j) order; not written when
+ *                   an expert id is out of range
  *   stream          cudaStream_t; the call is asynchronous
  * Limits: T*k <= TOVL_NOALLOC_MAX_PAIRS and E <= TOVL_NOALLOC_MAX_EXPERTS;
  * larger sizes return TOVL_ERR_UNSUPPORTED before anything is enqueued.
  * It runs on the calling thread's current device.  The first call on a
  * device looks up the scratch array's device address (cudaGetSymbolAddress)
- * and keeps it; make that first call before any stream capture.  All calls
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture.  The kept address does not survive a reset of the device
+ * (cudaDeviceReset, or a reset of its primary context): after one, this
+ * entry point must not be called again in that process.  All calls
  * on a device share the one array and it keeps the previous call's
  * contents, so calls whose kernels overlap on the GPU (other streams, other
  * threads) race and must be serialised by the caller. */
@@ -285,7 +294,8 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * cooperative launches are accepted with pairs (read only), 13 = fused
  * launches request the cooperative co-residency guarantee (1, the default;
  * 0 launches the same kernel without it, for tools that cannot replay
- * cooperative launches -- the grid still fits one CTA per SM),
+ * cooperative launches -- the grid still fits one CTA per SM; the same
+ * switch applies to the combine kernel and to gated copies),
  * 14 = producer copy path of the fused kernels: 0 = 16-byte vector loads and
  * stores through registers (the default), 1 = bulk asynchronous loads of each
  * row segment into a per-warp shared-memory buffer, then 16-byte vector
@@ -325,6 +335,19 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * producer CTAs and single-CTA tiles (uniform 141.5 -> 118 us, Zipf 793 ->
  * 670 us), the TP gather 4-6 % slower (its three tile waves
  * stay three; the copy warps share the SMs),
+ * 19 = where tovl_gemm_reduce_scatter sums the partials: 0 (the default) =
+ * producer CTAs reduce, consumers join them when option 16 is on; 1 (when no
+ * producer count is set) = every SM computes partial tiles and the CTA pair
+ * that computes shard (o mod S)'s partial of output tile o sums that tile's S
+ * partials in six otherwise idle warps, once all S partial tiles' slots are
+ * published,
+ * 20 = L2 eviction priorities of the fused calls' memory streams, a bit mask:
+ * 1 producer source loads evict-last, 32 evict-first; 16 producer
+ * destination stores evict-last; 4 A tensor loads evict-first; 8 weight
+ * tensor loads evict-last; 2 output tensor stores evict-first; 0 = no
+ * priorities; -1 (the default) = each call's measured choice: 32 | 8 for
+ * tovl_gather_gemm, 8 for tovl_dispatch_grouped_gemm, 0 otherwise (results
+ * are identical whatever the mask),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in

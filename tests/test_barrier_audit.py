@@ -18,7 +18,8 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 # functions that run after the role split: no CTA-wide barrier may appear
 ROLE_FUNCTIONS = {
     "consumer.cuh": ["consumer_tma", "consumer_mma", "consumer_epilogue", "gate", "consumer_gate", "wait_gate", "embedded_producer"],
-    "producer.cuh": ["seed_counters", "begin_item", "load_pass", "store_pass", "copy_items", "copy_items_staged", "rs_reduce"],
+    "producer.cuh": ["seed_counters", "begin_item", "load_pass", "store_pass", "copy_items", "copy_items_staged", "rs_reduce",
+                     "rs_reduce_owned"],
     "copyplane.cuh": ["bulk_stream", "run_bulk"],
     "copy.cu": ["copy_v4", "copy_waiter", "copy_seeds"],
 }

@@ -360,6 +360,27 @@ def test_combine_shapes(T, k, E):
         _check_ctrl(h, 2)
 
 
+@pytest.mark.parametrize("T,k,E", [(40, 67, 8), (9, 130, 5), (3, 2100, 4)])
+def test_combine_tokens_spanning_many_chunks(T, k, E):
+    # a token's k staged rows span three or more 64-row chunks (k = 67, 130),
+    # and more than 32 of them (k = 2100): the reducer must wait on every one
+    # of those chunk slots, not only the first and the last.  Experts are
+    # drawn with replacement, so a token may name one expert many times.
+    H, N = 64, 128
+    with _handle(max_rows=1 << 14, max_pairs=1 << 14) as h:
+        for r in (1, 2):
+            topk_np = workloads.repeated_topk(T, k, E, workloads.round_seed(7, r))
+            x = workloads.bf16_normal((T, H), 1.0, 70 + r, DEV)
+            W = workloads.bf16_normal((E, H, 256), 1.0, 80 + r, DEV)
+            _dispatch_round(h, x, topk_np, W)
+            y, w_np, staging, combined = _combine_round(h, tovl.dispatch_rows(T, k, E), N, T, k, 90 + r)
+            assert h.sync_status() == 0
+            S, C = oracle.combine(bits(y), oracle.dispatch_plan(topk_np, E).dst, w_np)
+            assert np.array_equal(bits(staging[:T * k]), S), f"staging, round {r}"
+            assert np.array_equal(bits(combined[:T]), C), f"combined, round {r}"
+            _check_ctrl(h, 2 * r)
+
+
 def test_moe_layer_dispatch_gemm_combine():
     # the whole layer against the oracle's: dispatch, grouped GEMM, combine
     T, H, k, E, N = 300, 256, 2, 6, 512
@@ -433,10 +454,32 @@ def test_gemm_reduce_scatter(S, M, Ks, N, P, pairs):
             _check_ctrl(h, r)
 
 
+@pytest.mark.parametrize("S,M,Ks,N", [(4, 512, 256, 512), (3, 384, 192, 768), (5, 256, 64, 256),
+                                      (40, 256, 64, 256), (2, 1024, 512, 1024)])
+@pytest.mark.parametrize("epi", [1, 0])
+def test_gemm_reduce_scatter_reducer_placement(S, M, Ks, N, epi):
+    # epi 1: the computer of shard (o mod S)'s partial of output tile o sums
+    # the tile in its idle warps, no producer CTAs; epi 0 (the default):
+    # producer CTAs reduce.  S = 40 makes a reducer poll more than 32 slots.
+    with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_RS_EPILOGUE, epi)
+        for r in range(1, 3):
+            X, W, partials, out = _rs_round(h, S, M, Ks, N, 900 + r)
+            assert h.sync_status() == 0
+            if epi:
+                assert h.get_option(tovl.OPT_PRODUCERS) == 0, "the epilogue reduction launches no producer CTAs"
+            Po, Oo = oracle.gemm_reduce_scatter(bits(X), bits(W))
+            for s in range(S):
+                assert_close(partials[s], oracle.bf16_to_f32(Po[s]), f"partial {s}")
+            assert_close(out, oracle.bf16_to_f32(Oo), "reduced")
+            _check_ctrl(h, r)
+
+
 @pytest.mark.parametrize("S,M,Ks,N,P", [(4, 512, 256, 512, 0), (3, 384, 192, 768, 4)])
 def test_gemm_reduce_scatter_without_role_switch(S, M, Ks, N, P):
     with _handle(producer_ctas=P, k_slices=4) as h:
         h.set_option(tovl.OPT_ROLE_SWITCH, 0)
+        h.set_option(tovl.OPT_RS_EPILOGUE, 0)
         for r in range(1, 3):
             X, W, partials, out = _rs_round(h, S, M, Ks, N, 800 + r)
             assert h.sync_status() == 0
