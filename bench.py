@@ -651,7 +651,7 @@ def rs_bench(cfg, rounds: int, dev, producers_sweep=(0, 8, 16, 24, 32, 48), role
 def copy_sweep(rounds: int, dev, sizes, rounds_other: int = 20):
     """Gated and ungated permuted copies of 2^20 rows at every row size:
     `rounds` timed rounds (sequences advance every gated round) in the default
-    vector mode, `rounds_other` in the bulk mode."""
+    automatic mode, `rounds_other` in the vector and bulk modes."""
     import numpy as np
     import torch
     import workloads
@@ -670,10 +670,10 @@ def copy_sweep(rounds: int, dev, sizes, rounds_other: int = 20):
         for rb in sizes:
             src = src_all[: n * rb].view(n, rb)
             dst = dst_all[: n * rb].view(n, rb)
-            for mode in (tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK):
+            for mode in (tovl.TOVL_COPY_AUTO, tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK):
                 h.set_option(tovl.OPT_COPY_MODE, mode)
-                row = {"row_bytes": rb, "copy_mode": "vector" if mode == 0 else "bulk"}
-                nr = rounds if mode == tovl.TOVL_COPY_VECTOR else rounds_other
+                row = {"row_bytes": rb, "copy_mode": {0: "vector", 1: "bulk", 2: "auto"}[mode]}
+                nr = rounds if mode == tovl.TOVL_COPY_AUTO else rounds_other
                 row["rounds"] = nr
                 for gated in (False, True):
                     fn = lambda: h.gated_copy(src, dst, perm, gated=gated)  # noqa: E731
@@ -691,7 +691,8 @@ def copy_sweep(rounds: int, dev, sizes, rounds_other: int = 20):
                 row["signal_wait_us_p99"] = float(np.percentile(lat, 99))
                 res.append(row)
     return {"workload": cfg.name, "rows": n, "rounds": rounds, "rounds_bulk": rounds_other,
-            "default_copy_mode": "vector", "l2": "inputs larger than L2 (no flush)", "sweep": res}
+            "default_copy_mode": "auto (vector below 8 KB rows, bulk from 8 KB)",
+            "l2": "inputs larger than L2 (no flush)", "sweep": res}
 
 
 def run_tovl(args):
@@ -784,9 +785,9 @@ def run_tovl(args):
                    "producer_ctas": acc["producer_ctas"], "consumer_ctas": acc["consumer_ctas"],
                    "k_slices": args.k_slices},
         "overlap_efficiency": acc["overlap_efficiency"],
-        "gated_copy_GBps": (min(r["gated_GBps"] for r in extra["gated_copy"]["sweep"] if r["copy_mode"] == "vector")
+        "gated_copy_GBps": (min(r["gated_GBps"] for r in extra["gated_copy"]["sweep"] if r["copy_mode"] == "auto")
                             if "gated_copy" in extra else None),
-        "gated_copy_note": "lowest gated GB/s over the row sizes 256 B - 16 KB, default (vector) mode",
+        "gated_copy_note": "lowest gated GB/s over the row sizes 256 B - 16 KB, default (auto) mode",
         "acceptance": acc,
         "unfused_context": context,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,

@@ -373,21 +373,6 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     }
 }
 
-// Reduce-scatter: publish partial tile t once this warp's bulk store groups
-// other than the newest LEFT are complete (LEFT = 0: all of them).
-template <int PAIR, int LEFT>
-__device__ __forceinline__ void rs_publish(const FusedParams& p, int t, uint32_t lane)
-{
-    if (lane == 0) {
-        ptx::bulk_wait<LEFT>();
-        ptx::fence_proxy_async_global();
-    }
-    __syncwarp();
-    static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
-    if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
-    __syncwarp();
-}
-
 // Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) ->
 // shared memory -> TMA tensor store.  Warp w reads TMEM lane quarter w % 4
 // (the quarter its position allows), i.e. 32 output rows, and one half of
@@ -396,8 +381,11 @@ __device__ __forceinline__ void rs_publish(const FusedParams& p, int t, uint32_t
 // map expects (16-byte chunk j of 64-byte row r at chunk j ^ ((r / 2) % 4):
 // the eight rows a quarter-warp writes hit distinct banks), then one lane
 // stores it; rows past the output's extent (the ragged tail of M) are
-// clipped by the store.  The accumulator is released as soon as its last
-// columns are in registers.
+// clipped by the store.  Reduce-scatter partial tiles instead leave the
+// buffer through the warp's own 16-byte stores (their epilogues come every
+// few microseconds, and a tensor store holds its buffer for about a
+// microsecond).  The accumulator is released as soon as its last columns are
+// in registers.
 template <int PAIR>
 __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                   uint32_t tmem_base)
@@ -410,8 +398,11 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
     const uint64_t pol_out = stream_policy(p, 0, kHintOutFirst);
-    constexpr int kBoxes = kTileN / 2 / kEpiBoxCols;   // TMA store groups per tile and warp
-    int pending = -1;    // reduce-scatter: the tile whose stores are in flight, published one tile later
+    // reduce-scatter tiles are short (K / S deep) and published one by one:
+    // their boxes leave shared memory through this warp's own coalesced
+    // stores, so no box waits for a tensor store to finish reading its buffer
+    const bool gstore = p.mode == kModeReduceScatter;
+    const uint32_t buf_addr = ptx::smem_u32(buf);
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const int arow = sc.a_row(p, t);
@@ -438,7 +429,7 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
 #pragma unroll 1
         for (int bx = 0; bx < kTileN / 2 / kEpiBoxCols; ++bx) {
             // the previous store from this buffer has finished reading it
-            if (lane == 0) ptx::bulk_wait_read<0>();
+            if (!gstore && lane == 0) ptx::bulk_wait_read<0>();
             __syncwarp();
             {
                 uint32_t r[32];
@@ -463,26 +454,45 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                     else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
                 }
             }
-            // the box's generic-proxy writes are visible to the tensor store
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                       arow + q * 32, pol_out);
-                ptx::bulk_commit();
+            if (gstore) {
+                // lane l writes 16-byte chunk l % 4 of box rows l / 4 + 8i:
+                // four lanes cover a row's 64 bytes (two full sectors)
+                __syncwarp();
+                const int col = nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = static_cast<int>(lane >> 2) + 8 * i;
+                    const uint32_t chunk = (lane & 3u) ^ ((static_cast<uint32_t>(rr) >> 1) & 3u);
+                    const int4 v = ptx::ld_shared_v4(buf_addr + static_cast<uint32_t>(rr) * (kEpiBoxCols * 2) + chunk * 16);
+                    const int row = arow + q * 32 + rr;
+                    if (row < p.out_rows)
+                        ptx::st_v4(reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) +
+                                                           (static_cast<size_t>(row) * p.N + col) * 2) + (lane & 3u),
+                                   v);
+                }
+                __syncwarp();   // the buffer is read before the next box overwrites it
+            } else {
+                // the box's generic-proxy writes are visible to the tensor store
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                           arow + q * 32, pol_out);
+                    ptx::bulk_commit();
+                }
             }
         }
         if (p.mode == kModeReduceScatter) {
-            // Publish the previous partial tile ("cross-GPU sync protocols on
-            // PCIe", section 3): once this warp's stores of it have written
-            // global memory -- every bulk group but this tile's kBoxes is
-            // complete -- it arrives on that tile's counter with its share of
-            // the 64-unit quota; the arrival that completes the count is
-            // elected and release-stores the sequence into the tile's slot.
-            // Publishing one tile late keeps the wait for store completion
-            // off the path from one accumulator drain to the next.
-            if (pending >= 0) rs_publish<PAIR, kBoxes>(p, pending, lane);
-            pending = t;
+            // Publish the partial tile ("cross-GPU sync protocols on PCIe",
+            // section 3): the warp's stores of it come before lane 0's
+            // acq_rel arrival on the tile's counter with the warp's share of
+            // the 64-unit quota (warp barrier, then the release); the arrival
+            // that completes the count is elected and release-stores the
+            // sequence into the tile's slot.
+            static_assert(kChunkRows % (kEpiWarps * PAIR) == 0, "warp shares must sum to the chunk quota");
+            __syncwarp();
+            if (lane == 0) arrive_and_publish(p.ctrl, t, kChunkRows / (kEpiWarps * PAIR), p.seq);
+            __syncwarp();
         }
         if (p.stats && lane == 0) {
             const long long idx = static_cast<long long>(p.trace_tiles) * p.k_slices + t;
@@ -490,8 +500,6 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                 atomicMax(reinterpret_cast<unsigned long long*>(p.ctrl.trace + idx), ptx::globaltimer());
         }
     }
-    // the last partial tile: all its stores complete, then published
-    if (pending >= 0) rs_publish<PAIR, 0>(p, pending, lane);
     // every store has written global memory before the CTA retires
     if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();

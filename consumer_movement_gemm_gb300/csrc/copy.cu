@@ -23,17 +23,6 @@ constexpr int kCopyThreads = 512;
 constexpr int kCopyUnroll = 8;
 constexpr int kCopySmem = 200 * 1024;
 
-__device__ __forceinline__ void chunk_arrive(const CopyParams& p, long long dst_row)
-{
-    const int c = static_cast<int>(dst_row / kChunkRows);
-    const int cs = c * p.ctrl.n_slices;            // a copy is not sliced: slice 0 carries the rows
-    const int old = ptx::atom_add_acq_rel_gpu(p.ctrl.cnt + cs, 1);
-    if (old + 1 == p.seq * kChunkRows) {
-        if (p.stamps) p.ctrl.pub_ns[c] = static_cast<long long>(ptx::globaltimer());
-        ptx::st_release_gpu(p.ctrl.slot + cs, p.seq);
-    }
-}
-
 // The elected arrival of chunk c (its relaxed add completed the count):
 // acquire every earlier arrival, then publish the round's sequence.
 __device__ __forceinline__ void publish_chunk(const CopyParams& p, int c)
@@ -118,25 +107,6 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
     }
 }
 
-struct PermRowJob {
-    const CopyParams* p;
-    long long cursor;
-    long long step;
-    __device__ int next()
-    {
-        if (cursor >= p->n_rows) return -1;
-        const long long r = cursor;
-        cursor += step;
-        return static_cast<int>(r);
-    }
-    __device__ const void* src(int r) { return p->src + static_cast<long long>(r) * p->row_bytes; }
-    __device__ void* dst(int r) { return p->dst + static_cast<long long>(p->perm[r]) * p->row_bytes; }
-    __device__ void done(int r)
-    {
-        if (p->gated) chunk_arrive(*p, p->perm[r]);
-    }
-};
-
 // Waiters: warp w watches chunks [w*per, (w+1)*per); lane i of the warp owns
 // chunks c = base + i + 32*j.  A lane re-polls only chunks it has not seen.
 // Eight slots per lane are read per pass with relaxed (strong) loads, so the
@@ -212,19 +182,16 @@ __global__ void __launch_bounds__(kCopyThreads, 2) copy_kernel(const __grid_cons
         copy_v4(p, blockIdx.x * n_warps + warp, p.n_copiers * n_warps);
         return;
     }
-    // bulk mode: lane 0 of four warps each runs an issuer over a quarter of
-    // the shared memory
+    // bulk mode: four warps each stream rows through a quarter of the shared
+    // memory (lane 0 issues the copies; the warp prefetches destinations and
+    // counts retired rows 32 at a time)
     constexpr int kIssuers = 4;
     if (warp < kIssuers) {
-        if (ptx::lane_id() == 0) {
-            uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-            const int share = (kCopySmem - 1024) / kIssuers / 1024 * 1024;
-            const Ring ring = make_ring(smem + warp * share, share, p.row_bytes);
-            PermRowJob job{&p, static_cast<long long>(blockIdx.x) * kIssuers + warp,
-                           static_cast<long long>(p.n_copiers) * kIssuers};
-            run_bulk(job, static_cast<uint32_t>(p.row_bytes), ring, p.ctrl, p.pipe_timeout_ns);
-        }
-        __syncwarp();
+        uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        const int share = (kCopySmem - 1024) / kIssuers / 1024 * 1024;
+        const Ring ring = make_ring(smem + warp * share, share, p.row_bytes);
+        run_bulk(p, static_cast<long long>(blockIdx.x) * kIssuers + warp, static_cast<long long>(p.n_copiers) * kIssuers,
+                 ring, p.pipe_timeout_ns);
     }
 }
 

@@ -26,6 +26,7 @@ cudaError_t prepare_copy();
 int copy_max_active_per_sm(int copy_mode);
 int copy_bulk_max_row_bytes();
 constexpr int kCopyWarpsPerCta = 16;
+constexpr int kCopyAutoBulkRowBytes = 8192;    // TOVL_COPY_AUTO takes bulk copies from this row size
 constexpr int kWaiterChunksPerWarp = 8 * 32;   // one pass of eight slots per lane
 
 }  // namespace tovl

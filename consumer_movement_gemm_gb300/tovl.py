@@ -23,6 +23,7 @@ TOVL_ERR_TIMEOUT = 4
 TOVL_ERR_OOM = 5
 TOVL_COPY_VECTOR = 0
 TOVL_COPY_BULK = 1
+TOVL_COPY_AUTO = 2
 
 OPT_PRODUCERS = 1
 OPT_CONSUMERS = 2

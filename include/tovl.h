@@ -57,7 +57,8 @@ typedef enum {
  * kernels use 16 warps per CTA; their copy path is option 14. */
 typedef enum {
     TOVL_COPY_VECTOR = 0,      /* 16-byte vector loads/stores by warps */
-    TOVL_COPY_BULK = 1         /* bulk asynchronous copies through a shared-memory ring */
+    TOVL_COPY_BULK = 1,        /* bulk asynchronous copies through a shared-memory ring */
+    TOVL_COPY_AUTO = 2         /* vector below 8 KB rows, bulk from 8 KB (the default) */
 } tovl_copy_mode;
 
 typedef struct {
@@ -69,8 +70,9 @@ typedef struct {
     int consumer_ctas;         /* C; 0 = all remaining SMs */
     long long wait_timeout_ns; /* bound of every device wait; 0 = 2 s */
     int copy_mode;             /* tovl_copy_mode of tovl_gated_copy; the default is
-                                  TOVL_COPY_VECTOR (measured on GB300: 71-91 % of the
-                                  HBM copy bandwidth gated, 256 B to 16 KB rows) */
+                                  TOVL_COPY_AUTO (measured on GB300, gated: 71-91 % of
+                                  the HBM copy bandwidth with vector copies from 256 B
+                                  to 4 KB rows, 94-96 % with bulk copies at 8-16 KB) */
     long long max_rows;        /* capacity in rows of gathered/dispatched buffers and copies */
     int max_pairs;             /* largest T*k of a dispatch call */
     int max_experts;           /* largest E of a dispatch call (<= 512) */

@@ -180,10 +180,12 @@ def test_gemm_reduce_scatter_full_size():
         _check_ctrl(h, 1)
 
 
-@pytest.mark.parametrize("row_bytes", [256, 1024, 8192, 16384])
-def test_gated_copy_full_size(row_bytes):
+@pytest.mark.parametrize("row_bytes,mode", [(256, 0), (1024, 0), (8192, 0), (16384, 0), (256, 1), (16384, 1),
+                                            (8192, 2)])
+def test_gated_copy_full_size(row_bytes, mode):
     # 2^20 permuted rows (256 B - 16 KB, up to 16 GiB each way), the copy
-    # line's handle and copy mode, two rounds
+    # line's handle in the vector (0), bulk (1) and default automatic (2)
+    # modes, two rounds
     cfg = workloads.COPY
     n, rb = cfg.n_rows, row_bytes
     perm_np = workloads.permutation(n, cfg.seed)
@@ -191,7 +193,7 @@ def test_gated_copy_full_size(row_bytes):
     rows = _rows(n, [0, n - 1], 2048, 7)
     dests = perm_np[rows].astype(np.int64)
     rank = np.argsort(np.argsort(dests)).astype(np.int32)
-    with tovl.Handle(0, max_rows=n) as h:
+    with tovl.Handle(0, max_rows=n, copy_mode=mode) as h:
         src = torch.empty(n, rb, dtype=torch.uint8, device=DEV)
         dst = torch.zeros_like(src)
         for r in (1, 2):

@@ -516,8 +516,11 @@ def test_gemm_reduce_scatter_rejects_shapes():
 # ------------------------------------------------------------------ gated copy
 @pytest.mark.parametrize("row_bytes", [256, 1024, 8192])
 @pytest.mark.parametrize("copy_mode", [tovl.TOVL_COPY_VECTOR, tovl.TOVL_COPY_BULK])
-def test_gated_copy_small(row_bytes, copy_mode):
-    n = 5000
+@pytest.mark.parametrize("n", [5000, 100, 20000])
+def test_gated_copy_small(row_bytes, copy_mode, n):
+    # 100 rows: most bulk issuer warps get no row; 20000 rows: about 33 rows per
+    # issuer, so every issuer counts one full batch of 32 retired rows and a
+    # partial one
     with _handle(copy_mode=copy_mode, max_rows=n, k_slices=2) as h:
         for r in range(1, 3):
             perm_np = workloads.permutation(n, r)
