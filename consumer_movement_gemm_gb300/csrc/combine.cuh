@@ -53,10 +53,13 @@ __device__ inline void reducer(const FusedParams& p, int rid, int n_units, int f
                 return;
         }
         // a lane's column groups are lane, lane + 32, ... below N / 8; kBatch
-        // of them are loaded together per staged row, so a token costs k
-        // round trips per batch instead of one per group (a group past the
-        // row loads the lane's first one again and is not stored)
+        // of them from kRows staged rows are loaded together (16 loads in
+        // flight per lane), so a token with k <= 4 costs one round trip per
+        // batch (a group past the row loads the lane's first one again and is
+        // not stored; a row past k re-reads the token's last row, whose
+        // product is skipped)
         constexpr int kBatch = 4;
+        constexpr int kRows = 4;
         const int per_lane = (groups + 31) / 32;
         for (int i0 = 0; i0 < per_lane; i0 += kBatch) {
             float acc[kBatch][8];
@@ -64,23 +67,33 @@ __device__ inline void reducer(const FusedParams& p, int rid, int n_units, int f
             for (int b = 0; b < kBatch; ++b)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) acc[b][c] = 0.0f;
-            for (int j = 0; j < p.k; ++j) {
-                const float w = p.gate_w[s0 + j];
-                const int4* row = reinterpret_cast<const int4*>(staging + (s0 + j) * row_bytes);
-                int4 v[kBatch];
+            for (int j0 = 0; j0 < p.k; j0 += kRows) {
+                float w[kRows];
+                int4 v[kRows][kBatch];
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const int g = lane + 32 * (i0 + b);
-                    v[b] = ptx::ld_v4(row + (g < groups ? g : lane % groups));
+                for (int jj = 0; jj < kRows; ++jj) {
+                    const int j = min(j0 + jj, p.k - 1);
+                    w[jj] = p.gate_w[s0 + j];
+                    const int4* row = reinterpret_cast<const int4*>(staging + static_cast<size_t>(s0 + j) * row_bytes);
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        const int g = lane + 32 * (i0 + b);
+                        v[jj][b] = ptx::ld_v4(row + (g < groups ? g : lane % groups));
+                    }
                 }
+                // products and sums in ascending j
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const uint32_t u[4] = {static_cast<uint32_t>(v[b].x), static_cast<uint32_t>(v[b].y),
-                                           static_cast<uint32_t>(v[b].z), static_cast<uint32_t>(v[b].w)};
+                for (int jj = 0; jj < kRows; ++jj) {
+                    if (j0 + jj >= p.k) break;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        acc[b][2 * c] = __fadd_rn(acc[b][2 * c], __fmul_rn(w, bf16_lo(u[c])));
-                        acc[b][2 * c + 1] = __fadd_rn(acc[b][2 * c + 1], __fmul_rn(w, bf16_hi(u[c])));
+                    for (int b = 0; b < kBatch; ++b) {
+                        const uint32_t u[4] = {static_cast<uint32_t>(v[jj][b].x), static_cast<uint32_t>(v[jj][b].y),
+                                               static_cast<uint32_t>(v[jj][b].z), static_cast<uint32_t>(v[jj][b].w)};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            acc[b][2 * c] = __fadd_rn(acc[b][2 * c], __fmul_rn(w[jj], bf16_lo(u[c])));
+                            acc[b][2 * c + 1] = __fadd_rn(acc[b][2 * c + 1], __fmul_rn(w[jj], bf16_hi(u[c])));
+                        }
                     }
                 }
             }
