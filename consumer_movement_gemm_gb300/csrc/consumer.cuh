@@ -373,6 +373,36 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     }
 }
 
+// One 32 x 32 box of accumulator values (this lane's row, 32 columns) to the
+// output through the warp's staging buffer and coalesced 16-byte stores: four
+// lanes cover a row's 64 bytes.
+__device__ __forceinline__ void gstore_box(const FusedParams& p, uint32_t row_addr, uint32_t buf_addr, uint32_t swz,
+                                           uint32_t lane, int row0, int col, const uint32_t (&r)[32])
+{
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint32_t chunk = static_cast<uint32_t>(v) ^ swz;
+        ptx::st_shared_v4(row_addr + chunk * 16,
+                          ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                          ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                          ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                          ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rr = static_cast<int>(lane >> 2) + 8 * i;
+        const uint32_t chunk = (lane & 3u) ^ ((static_cast<uint32_t>(rr) >> 1) & 3u);
+        const int4 v = ptx::ld_shared_v4(buf_addr + static_cast<uint32_t>(rr) * (kEpiBoxCols * 2) + chunk * 16);
+        const int row = row0 + rr;
+        if (row < p.out_rows)
+            ptx::st_v4(reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) + (static_cast<size_t>(row) * p.N + col) * 2) +
+                           (lane & 3u),
+                       v);
+    }
+    __syncwarp();   // the buffer is read before the next box overwrites it
+}
+
 // Epilogue warps: TMEM -> registers -> bf16 (round to nearest even) ->
 // shared memory -> TMA tensor store.  Warp w reads TMEM lane quarter w % 4
 // (the quarter its position allows), i.e. 32 output rows, and one half of
@@ -426,10 +456,32 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             continue;
         }
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
+        if (gstore) {
+            // two boxes' accumulator loads in flight per wait
+            const int col0 = nb * kTileN + half * (kTileN / 2);
+#pragma unroll
+            for (int b2 = 0; b2 < kTileN / 2 / kEpiBoxCols; b2 += 2) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(taddr + b2 * kEpiBoxCols, r0);
+                ptx::tmem_ld_32x32b_x32(taddr + (b2 + 1) * kEpiBoxCols, r1);
+                ptx::tmem_ld_wait();
+                if (b2 + 2 == kTileN / 2 / kEpiBoxCols) {
+                    // this warp's reads of the accumulator are done: one arrival per warp
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (PAIR == 1) ptx::mbar_arrive(&s.tempty[acc]);
+                        else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
+                    }
+                }
+                gstore_box(p, row_addr, buf_addr, swz, lane, arow + q * 32, col0 + b2 * kEpiBoxCols, r0);
+                gstore_box(p, row_addr, buf_addr, swz, lane, arow + q * 32, col0 + (b2 + 1) * kEpiBoxCols, r1);
+            }
+        }
 #pragma unroll 1
-        for (int bx = 0; bx < kTileN / 2 / kEpiBoxCols; ++bx) {
+        for (int bx = 0; bx < (gstore ? 0 : kTileN / 2 / kEpiBoxCols); ++bx) {
             // the previous store from this buffer has finished reading it
-            if (!gstore && lane == 0) ptx::bulk_wait_read<0>();
+            if (lane == 0) ptx::bulk_wait_read<0>();
             __syncwarp();
             {
                 uint32_t r[32];
@@ -454,32 +506,13 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                     else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
                 }
             }
-            if (gstore) {
-                // lane l writes 16-byte chunk l % 4 of box rows l / 4 + 8i:
-                // four lanes cover a row's 64 bytes (two full sectors)
-                __syncwarp();
-                const int col = nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rr = static_cast<int>(lane >> 2) + 8 * i;
-                    const uint32_t chunk = (lane & 3u) ^ ((static_cast<uint32_t>(rr) >> 1) & 3u);
-                    const int4 v = ptx::ld_shared_v4(buf_addr + static_cast<uint32_t>(rr) * (kEpiBoxCols * 2) + chunk * 16);
-                    const int row = arow + q * 32 + rr;
-                    if (row < p.out_rows)
-                        ptx::st_v4(reinterpret_cast<int4*>(static_cast<uint8_t*>(p.out) +
-                                                           (static_cast<size_t>(row) * p.N + col) * 2) + (lane & 3u),
-                                   v);
-                }
-                __syncwarp();   // the buffer is read before the next box overwrites it
-            } else {
-                // the box's generic-proxy writes are visible to the tensor store
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                           arow + q * 32, pol_out);
-                    ptx::bulk_commit();
-                }
+            // the box's generic-proxy writes are visible to the tensor store
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
+                                       arow + q * 32, pol_out);
+                ptx::bulk_commit();
             }
         }
         if (p.mode == kModeReduceScatter) {

@@ -52,7 +52,8 @@ __device__ void copy_seeds(const CopyParams& p, int tid, int n_threads)
 
 // Vector copy: each warp takes a group of consecutive source rows (about
 // 16 KB) and moves it as one flat range of 16-byte words, kCopyUnroll words
-// in flight per lane; then one lane per row counts the row.
+// in flight per lane, the group's destination rows loaded once up front;
+// then one lane per row counts the row.
 __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
 {
     const uint32_t lane = ptx::lane_id();
@@ -63,6 +64,10 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
         const long long r0 = g * rows_per_group;
         const int nr = static_cast<int>(min(static_cast<long long>(rows_per_group), p.n_rows - r0));
         const int total = nr * n16;
+        // destination rows of the group's rows, loaded once: lane l holds
+        // those of rows l and l + 32, and the stores take them by shuffle
+        const int pd0 = static_cast<int>(lane) < nr ? p.perm[r0 + lane] : 0;
+        const int pd1 = static_cast<int>(lane) + 32 < nr ? p.perm[r0 + lane + 32] : 0;
         for (int base = 0; base < total; base += 32 * kCopyUnroll) {
             int4 v[kCopyUnroll];
 #pragma unroll
@@ -76,9 +81,11 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
 #pragma unroll
             for (int j = 0; j < kCopyUnroll; ++j) {
                 const int idx = base + j * 32 + static_cast<int>(lane);
+                const int rr = idx / n16, cc = idx - rr * n16;
+                const int d0 = __shfl_sync(0xffffffffu, pd0, rr & 31);
+                const int d1 = __shfl_sync(0xffffffffu, pd1, rr & 31);
                 if (idx < total) {
-                    const int rr = idx / n16, cc = idx - rr * n16;
-                    const long long d = p.perm[r0 + rr];
+                    const long long d = rr < 32 ? d0 : d1;
                     ptx::st_v4(reinterpret_cast<int4*>(p.dst + d * p.row_bytes) + cc, v[j]);
                 }
             }
@@ -94,11 +101,11 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
             const int S = p.ctrl.n_slices;
             int c0 = -1, c1 = -1, o0 = 0, o1 = 0;
             if (static_cast<int>(lane) < nr) {
-                c0 = p.perm[r0 + lane] / kChunkRows;
+                c0 = pd0 / kChunkRows;
                 o0 = ptx::atom_add_relaxed_gpu(p.ctrl.cnt + c0 * S, 1);
             }
             if (static_cast<int>(lane) + 32 < nr) {
-                c1 = p.perm[r0 + lane + 32] / kChunkRows;
+                c1 = pd1 / kChunkRows;
                 o1 = ptx::atom_add_relaxed_gpu(p.ctrl.cnt + c1 * S, 1);
             }
             if (c0 >= 0 && o0 + 1 == p.seq * kChunkRows) publish_chunk(p, c0);
