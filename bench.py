@@ -808,7 +808,7 @@ def run_profile(args):
     calls of one kernel, nothing else timed.
       fused     tovl_gather_gemm on the TP shape (about 110 MB resident)
       gemm      tovl_gemm_only on the TP shape
-      copy      tovl_gated_copy, 2^18 rows x 8 KB, gated (4 GB resident)
+      copy      tovl_gated_copy, 2^18 rows x 8 KB, gated, default copy mode (4 GB resident)
       dispatch  tovl_dispatch_grouped_gemm on the uniform top-2 workload
       combine   the dispatch calls, each followed by tovl_combine
       rs        tovl_gemm_reduce_scatter on the TP shape split four ways along K"""
@@ -836,7 +836,7 @@ def run_profile(args):
         perm = torch.from_numpy(workloads.permutation(rows, 0)).to(dev)
         src = workloads.random_bytes(rows, rb, 0, dev)
         dst = torch.empty_like(src)
-        with tovl.Handle(0, max_rows=rows, copy_mode=tovl.TOVL_COPY_VECTOR) as h:
+        with tovl.Handle(0, max_rows=rows) as h:      # the default (automatic) copy mode: bulk at 8 KB rows
             for _ in range(n):
                 h.gated_copy(src, dst, perm, gated=True)
             assert h.sync_status() == 0
