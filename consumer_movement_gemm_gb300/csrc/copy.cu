@@ -52,11 +52,14 @@ __device__ void copy_seeds(const CopyParams& p, int tid, int n_threads)
 
 // Vector copy: each warp takes a group of consecutive source rows (about
 // 16 KB) and moves it as one flat range of 16-byte words, kCopyUnroll words
-// in flight per lane, the group's destination rows loaded once up front;
-// then one lane per row counts the row.
+// in flight per lane, the group's destination rows loaded once up front
+// into a per-warp table in shared memory; then one lane per row counts the
+// row.
 __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
 {
+    __shared__ int dst_tabs[kCopyThreads / 32][64];
     const uint32_t lane = ptx::lane_id();
+    int* dst_tab = dst_tabs[threadIdx.x / 32];
     const int n16 = p.row_bytes / 16;
     const int rows_per_group = min(64, max(1, 16384 / p.row_bytes));   // at most two rows per lane
     const long long n_groups = (p.n_rows + rows_per_group - 1) / rows_per_group;
@@ -64,10 +67,14 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
         const long long r0 = g * rows_per_group;
         const int nr = static_cast<int>(min(static_cast<long long>(rows_per_group), p.n_rows - r0));
         const int total = nr * n16;
-        // destination rows of the group's rows, loaded once: lane l holds
-        // those of rows l and l + 32, and the stores take them by shuffle
+        // destination rows of the group's rows, loaded once (lane l those of
+        // rows l and l + 32) into the warp's 64-entry table
         const int pd0 = static_cast<int>(lane) < nr ? p.perm[r0 + lane] : 0;
         const int pd1 = static_cast<int>(lane) + 32 < nr ? p.perm[r0 + lane + 32] : 0;
+        __syncwarp();          // the previous group's stores have read the table
+        dst_tab[lane] = pd0;
+        dst_tab[lane + 32] = pd1;
+        __syncwarp();
         for (int base = 0; base < total; base += 32 * kCopyUnroll) {
             int4 v[kCopyUnroll];
 #pragma unroll
@@ -81,11 +88,9 @@ __device__ void copy_v4(const CopyParams& p, int gw, int n_gw)
 #pragma unroll
             for (int j = 0; j < kCopyUnroll; ++j) {
                 const int idx = base + j * 32 + static_cast<int>(lane);
-                const int rr = idx / n16, cc = idx - rr * n16;
-                const int d0 = __shfl_sync(0xffffffffu, pd0, rr & 31);
-                const int d1 = __shfl_sync(0xffffffffu, pd1, rr & 31);
                 if (idx < total) {
-                    const long long d = rr < 32 ? d0 : d1;
+                    const int rr = idx / n16, cc = idx - rr * n16;
+                    const long long d = dst_tab[rr];
                     ptx::st_v4(reinterpret_cast<int4*>(p.dst + d * p.row_bytes) + cc, v[j]);
                 }
             }
