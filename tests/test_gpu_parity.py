@@ -680,3 +680,25 @@ def test_dispatch_embedded_producers(routing, align):
             assert np.array_equal(bits(dispatched[:m_pad]), D), "dispatched buffer"
             assert_close(out[:m_pad], oracle.grouped_matmul_f32(D, bits(W), p.off), "embedded producers")
             _check_ctrl(h, r)
+
+
+@pytest.mark.parametrize("mask", [0, 1, 2, 4, 8, 16, 32, 63])
+def test_l2_eviction_hints_leave_results_unchanged(mask):
+    # option 20 only changes L2 eviction priorities: the gather + GEMM and the
+    # dispatch + grouped GEMM agree with the oracle under every hint bit
+    cfg = workloads.GatherCfg("hints", 3, 200, 320, 512, rounds=2)
+    with _handle(producer_ctas=6, k_slices=2) as h:
+        h.set_option(tovl.OPT_L2_HINTS, mask)
+        assert h.get_option(tovl.OPT_L2_HINTS) == mask
+        X, W, gathered, out = _gather_round(h, cfg, 40 + mask)
+        assert h.sync_status() == 0
+        G = oracle.gather([bits(X[s]) for s in range(cfg.shards)])
+        assert np.array_equal(bits(gathered), G)
+        assert_close(out, oracle.matmul_f32(G, bits(W)), f"gather, hints {mask}")
+        topk_np, E = ROUTINGS["zipf"](workloads.round_seed(9, mask))
+        T = topk_np.shape[0]
+        x = workloads.bf16_normal((T, 192), 1 / math.sqrt(192), 50 + mask, DEV)
+        Wd = workloads.bf16_normal((E, 192, 256), 1 / math.sqrt(192), 60 + mask, DEV)
+        dispatched, offs, outd = _dispatch_round(h, x, topk_np, Wd)
+        assert h.sync_status() == 0
+        _check_dispatch(h, x, topk_np, Wd, dispatched, offs, outd, 2)
