@@ -12,9 +12,13 @@
 //   warp 10     gate: polls the protocol (acquire loads of local slots /
 //               counters, ballot) ahead of the TMA warp and hands each
 //               passed gate over through shared memory
+//   warps 11-15 idle, or the embedded producers' copy warps (launches
+//               without producer CTAs), or the owners' reducers of a
+//               reduce-scatter with option 19
 // PAIR = 1: 128x256 tiles, stage = A 16 KB + B 32 KB, 4 stages.
 // PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
-// own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 6 stages); the
+// own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 5 stages beside
+// producer CTAs, 6 without); the
 // pair's first CTA issues the MMAs, which read A and B halves from both CTAs
 // and accumulate each CTA's rows in its own TMEM.  Both CTAs' TMA loads are
 // counted on the first CTA's "full" barriers; MMA completion is multicast to

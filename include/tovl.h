@@ -258,7 +258,10 @@ int tovl_copy_only(tovl_handle h, const void* const* shards, int num_shards, int
  *               slots (a protocol round); 0: the same copy with no
  *               protocol (not a round)
  *   stamps      1: record publish and first-observe times per chunk
- *               (read them with tovl_read_latency) */
+ *               (read them with tovl_read_latency)
+ * The copy mechanism is the handle's copy mode (option 3): vector copies, bulk
+ * copies (rows up to 24 KB; larger rows return TOVL_ERR_UNSUPPORTED), or the
+ * default automatic choice by row size.  Results are identical in every mode. */
 int tovl_gated_copy(tovl_handle h, const void* src, void* dst, long long n_rows, int row_bytes, const int* perm,
                     int gated, int stamps, void* stream);
 
