@@ -12,9 +12,12 @@
 //   warp 10     gate: polls the protocol (acquire loads of local slots /
 //               counters, ballot) ahead of the TMA warp and hands each
 //               passed gate over through shared memory
-//   warps 11-15 idle, or the embedded producers' copy warps (launches
-//               without producer CTAs), or the owners' reducers of a
-//               reduce-scatter with option 19
+//   warps 11-14 idle, or the embedded producers' copy warps (launches
+//               without producer CTAs), or (with warp 10) the owners'
+//               reducers of a reduce-scatter with option 19
+//   warp 15     stage waiter: observes each stage's full barrier and hands
+//               the stage to the MMA warp on a named barrier (fixed
+//               schedule; the dynamic schedule's MMA lane waits itself)
 // PAIR = 1: 128x256 tiles, stage = A 16 KB + B 32 KB, 4 stages.
 // PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
 // own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 5 stages beside
@@ -330,50 +333,93 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     }
 }
 
-// MMA warp: one lane (of the pair's first CTA) issues the MMAs.
+// MMA warp (of the pair's first CTA): lane 0 issues the MMAs.  The stages'
+// full barriers are observed by the stage waiter warp, which hands each
+// stage over on named barrier kStageBar0 + stage; the whole MMA warp takes
+// that barrier.  An mbarrier wait on the issuing thread itself stalls the
+// MMA stream even when the barrier has long completed (measured with pair
+// MMAs over five rotating stages: 128.7 clocks per MMA with no waits, 139.0
+// with one already-complete wait per k-block; 141.5 in the full handshake
+// against 129.6 with the hand-off).
 template <int PAIR, int ST>
 __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                              uint32_t tmem_base)
 {
     using T = Tile<PAIR, ST>;
-    if (ptx::lane_id() != 0 || sc.rank != 0) return;
-    uint32_t stage = 0, phase = 0;
+    if (sc.rank != 0) return;
+    const bool lead = ptx::lane_id() == 0;
+    uint32_t stage = 0;
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const uint32_t acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns)) return;
-        ptx::tc_fence_after();
+        if (lead) {
+            // a timeout is recorded in the status word; the loop goes on, so
+            // every stage hand-off of the waiter is still taken
+            mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.ctrl, p.pipe_timeout_ns);
+            ptx::tc_fence_after();
+        }
+        __syncwarp();
         const uint32_t d = tmem_base + acc * kTileN;
         for (int kb = 0; kb < p.n_kb; ++kb) {
-            // the stage's TMA bytes have landed (the barrier's transaction
-            // count); the MMAs below read them through the async proxy and
-            // are issued after this wait in program order.  No tcgen05
-            // thread-sync fence here: measured, it costs 14 clocks per MMA
-            // (142.5 instead of 128) once the stages rotate
-            if (!mbar_wait(&s.full[stage], phase, p.ctrl, p.pipe_timeout_ns)) return;
-            const uint32_t a0 = ptx::smem_u32(s.a + stage * T::kStageA);
-            const uint32_t b0 = ptx::smem_u32(s.b + stage * T::kStageB);
+            // the stage's TMA bytes have landed: the waiter observed its full
+            // barrier (the barrier's transaction count) and arrived here; the
+            // MMAs below read the stage through the async proxy.  No tcgen05
+            // thread-sync fence: measured, it costs 14 clocks per MMA
+            ptx::bar_sync_aligned(kStageBar0 + static_cast<int>(stage), kStageBarThreads);
+            if (lead) {
+                const uint32_t a0 = ptx::smem_u32(s.a + stage * T::kStageA);
+                const uint32_t b0 = ptx::smem_u32(s.b + stage * T::kStageB);
 #pragma unroll
-            for (int k = 0; k < kTileK / kUmmaK; ++k) {
-                // A: K-major, 128B swizzle; +32 B per 16-element k step inside
-                //    the swizzle row; 8-row groups 1024 B apart.
-                const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
-                // B: MN-major, 128B swizzle; +2048 B per 16 k-rows; 8-k-row
-                //    groups 1024 B apart; 64-column blocks 8 KB apart.
-                const uint64_t bd = ptx::smem_desc_sw128(b0 + k * 2048, kTileK * 128, 1024);
-                if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
-                else ptx::umma_bf16_pair(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                for (int k = 0; k < kTileK / kUmmaK; ++k) {
+                    // A: K-major, 128B swizzle; +32 B per 16-element k step inside
+                    //    the swizzle row; 8-row groups 1024 B apart.
+                    const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
+                    // B: MN-major, 128B swizzle; +2048 B per 16 k-rows; 8-k-row
+                    //    groups 1024 B apart; 64-column blocks 8 KB apart.
+                    const uint64_t bd = ptx::smem_desc_sw128(b0 + k * 2048, kTileK * 128, 1024);
+                    if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                    else ptx::umma_bf16_pair(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                }
+                if (PAIR == 1) ptx::umma_commit(&s.empty[stage]);
+                else ptx::umma_commit_pair(&s.empty[stage], 0x3);
             }
-            if (PAIR == 1) ptx::umma_commit(&s.empty[stage]);
-            else ptx::umma_commit_pair(&s.empty[stage], 0x3);
+            __syncwarp();
+            if (++stage == T::kStages) stage = 0;
+        }
+        if (lead) {
+            if (PAIR == 1) ptx::umma_commit(&s.tfull[acc]);
+            else ptx::umma_commit_pair(&s.tfull[acc], 0x3);
+        }
+        __syncwarp();
+    }
+}
+
+// Stage waiter warp (of the pair's first CTA): walks the MMA warp's k-block
+// sequence, lane 0 waits for each stage's full barrier, and the warp arrives
+// on the stage's named barrier.  A stage is refilled only after the MMA
+// warp's commit for its previous k-block, which follows the MMA warp's wait
+// on the same barrier, so no barrier id gets a second arrival before the MMA
+// warp has taken the first.  After a timeout lane 0 stops waiting but the
+// warp keeps arriving: the MMA warp never blocks on a named barrier.
+template <int PAIR, int ST>
+__device__ void consumer_stage_waiter(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
+{
+    using T = Tile<PAIR, ST>;
+    if (sc.rank != 0) return;
+    const bool lead = ptx::lane_id() == 0;
+    bool ok = true;
+    uint32_t stage = 0, phase = 0;
+    for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units) {
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+            if (lead && ok) ok = mbar_wait(&s.full[stage], phase, p.ctrl, p.pipe_timeout_ns);
+            __syncwarp();
+            ptx::bar_arrive_aligned(kStageBar0 + static_cast<int>(stage), kStageBarThreads);
             if (++stage == T::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        if (PAIR == 1) ptx::umma_commit(&s.tfull[acc]);
-        else ptx::umma_commit_pair(&s.tfull[acc], 0x3);
     }
 }
 
@@ -1010,7 +1056,7 @@ constexpr int kFirstCopyWarp = kGateWarp + 1;
 template <int PAIR>
 __device__ __forceinline__ void embedded_producer(const FusedParams& p)
 {
-    constexpr int kCopyWarps = kThreads / 32 - kFirstCopyWarp;
+    constexpr int kCopyWarps = kWaitWarp - kFirstCopyWarp;
     const int warp = threadIdx.x / 32;
     if (PAIR == 2) ptx::cluster_arrive_relaxed();
     ptx::grid_dep_wait();
@@ -1035,7 +1081,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     using T = Tile<PAIR, ST>;
     const int warp = threadIdx.x / 32;
     const ConsumerSmem<PAIR> s = consumer_smem<PAIR, ST>(smem);
-    if (EMB && warp >= kFirstCopyWarp) {
+    if (EMB && warp >= kFirstCopyWarp && warp < kWaitWarp) {
         embedded_producer<PAIR>(p);
         // the teardown barrier: TMEM is freed after every warp is done
         if (PAIR == 1) ptx::bar_sync_unaligned(0, kThreads);
@@ -1074,7 +1120,7 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
     // barriers initialised and TMEM allocated in both CTAs before any
     // cross-CTA arrival or load (copy warps only arrive)
     if (PAIR == 2) ptx::cluster_sync();
-    else if (EMB) ptx::bar_sync_unaligned(1, kFirstCopyWarp * 32);
+    else if (EMB) ptx::bar_sync_unaligned(1, (kFirstCopyWarp + 1) * 32);   // warps 0-10 and the waiter
     else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
@@ -1093,12 +1139,13 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         if (warp == 0) consumer_tma<PAIR, ST>(p, s, sc);
         else if (warp == 1) consumer_mma<PAIR, ST>(p, s, sc, tmem_base);
         else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
+        else if (warp == kWaitWarp) consumer_stage_waiter<PAIR, ST>(p, s, sc);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
         else if (warp >= kGateWarp && p.mode == kModeReduceScatter && p.rs_epi) {
             // no producer CTAs: the gate warp and the spare warps add the
             // per-round quota seeds of the counters this round does not fill,
             // then sum the output tiles this CTA (pair) owns
-            constexpr int kSpare = kThreads / 32 - kGateWarp;
+            constexpr int kSpare = kWaitWarp - kGateWarp;
             seed_counters(p, (warp - kGateWarp) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x),
                           kSpare * static_cast<int>(gridDim.x), false);
             rs_reduce_owned(p, sc.unit, sc.n_units, static_cast<int>(sc.rank), kGateWarp);

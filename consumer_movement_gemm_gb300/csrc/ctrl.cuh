@@ -19,10 +19,13 @@ constexpr int kTileN = 256;
 constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 5 spare (consumers) / 16 copy warps (producers)
+constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 4 spare, stage waiter (consumers) / 16 copy warps (producers)
 constexpr int kEpiWarp0 = 2;       // first epilogue warp
 constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, each owning 128 of the 256 columns
 constexpr int kGateWarp = 10;      // polls the protocol ahead of the TMA warp
+constexpr int kWaitWarp = 15;      // observes the stages' full barriers for the MMA warp (fixed schedule)
+constexpr int kStageBar0 = 2;      // named barrier kStageBar0 + stage: stage hand-off, waiter warp -> MMA warp
+constexpr int kStageBarThreads = 64;
 constexpr int kTraceCap = 1 << 20; // timeline entries kept when statistics are on
 constexpr int kMaxSlices = 8;      // K-slices per chunk watermark
 constexpr int kItemInt4 = 512;     // one producer item moves at most 8 KB per pass (16 x 16 B per lane)

@@ -424,7 +424,7 @@ static __device__ __noinline__ void rs_reduce_owned(const FusedParams& p, int un
 {
     const int lane = static_cast<int>(ptx::lane_id());
     const int w = static_cast<int>(threadIdx.x / 32) - first_warp;
-    const int n_warps = kThreads / 32 - first_warp;
+    const int n_warps = kWaitWarp - first_warp;   // warps first_warp .. kWaitWarp - 1
     const int S = p.n_shards;
     const int n_tiles = p.rs_tiles;
     const size_t row_bytes = static_cast<size_t>(p.N) * 2;

@@ -413,6 +413,18 @@ __device__ __forceinline__ void bar_sync_unaligned(int id, int n)
     asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// CTA barrier `id` over `n` threads, taken by every lane of the calling warp
+// at once (.aligned): wait for the barrier, or arrive without waiting.
+__device__ __forceinline__ void bar_sync_aligned(int id, int n)
+{
+    asm volatile("barrier.sync.aligned %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive_aligned(int id, int n)
+{
+    asm volatile("barrier.arrive.aligned %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {

@@ -333,7 +333,7 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * tovl_combine;
  * 2 = also in tovl_gather_gemm; 0 = off): the call launches no producer
  * CTAs; every SM (every co-resident CTA pair) is a consumer and the
- * consumer CTAs' five spare warps copy the rows, in the producers' order and
+ * consumer CTAs' four spare warps copy the rows, in the producers' order and
  * with their counters and seeds (16-byte vector copies whatever option 14
  * says; the role switch does not apply; CTA pairs on 128-row segments, see
  * 17).  Measured on GB300: dispatch calls 16-17 % shorter than with
@@ -344,7 +344,7 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * producer CTAs reduce, consumers join them when option 16 is on; 1 (when no
  * producer count is set) = every SM computes partial tiles and the CTA pair
  * that computes shard (o mod S)'s partial of output tile o sums that tile's S
- * partials in six otherwise idle warps, once all S partial tiles' slots are
+ * partials in five otherwise idle warps, once all S partial tiles' slots are
  * published,
  * 20 = L2 eviction priorities of the fused calls' memory streams, a bit mask:
  * 1 producer source loads evict-last, 32 evict-first; 16 producer
