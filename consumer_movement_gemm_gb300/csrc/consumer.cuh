@@ -222,20 +222,24 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
 {
     using T = Tile<PAIR, ST>;
     uint8_t* bdst = s.b + b.stage * T::kStageB;
+    // one 3-D load per kWBlocks 64-column blocks (measured: each tensor-load
+    // instruction stalls the MMA stream, two 2-D boxes per k-block cost 9.5
+    // clocks per pair MMA more than one 3-D box)
+    static_assert(T::kBBoxes % kWBlocks == 0, "whole weight loads per stage");
     if (PAIR == 1) {
         ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
 #pragma unroll
-        for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
-                                  b.brow + b.kb * kTileK, b.pol);
+        for (int j = 0; j < T::kBBoxes; j += kWBlocks)
+            ptx::tma_load_3d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], 0, b.brow + b.kb * kTileK,
+                                  b.n0 / 64 + j, b.pol);
     } else {
         // both CTAs' bytes are counted on the first CTA's barrier
         if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
 #pragma unroll
-        for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64,
-                                       b.brow + b.kb * kTileK, b.pol);
+        for (int j = 0; j < T::kBBoxes; j += kWBlocks)
+            ptx::tma_load_3d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, 0, b.brow + b.kb * kTileK,
+                                       b.n0 / 64 + j, b.pol);
     }
     ++b.issued;
     if (++b.stage == T::kStages) {
@@ -768,20 +772,24 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
 {
     using T = Tile<PAIR>;
     uint8_t* bdst = s.b + b.stage * T::kStageB;
+    // one 3-D load per kWBlocks 64-column blocks (measured: each tensor-load
+    // instruction stalls the MMA stream, two 2-D boxes per k-block cost 9.5
+    // clocks per pair MMA more than one 3-D box)
+    static_assert(T::kBBoxes % kWBlocks == 0, "whole weight loads per stage");
     if (PAIR == 1) {
         ptx::mbar_arrive_expect_tx(&s.full[b.stage], T::kStageBytes);
 #pragma unroll
-        for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], b.n0 + j * 64,
-                                  b.brow + b.kb * kTileK, b.pol);
+        for (int j = 0; j < T::kBBoxes; j += kWBlocks)
+            ptx::tma_load_3d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], 0, b.brow + b.kb * kTileK,
+                                  b.n0 / 64 + j, b.pol);
     } else {
         // both CTAs' bytes are counted on the first CTA's barrier
         if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
 #pragma unroll
-        for (int j = 0; j < T::kBBoxes; ++j)
-            ptx::tma_load_2d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, b.n0 + j * 64,
-                                       b.brow + b.kb * kTileK, b.pol);
+        for (int j = 0; j < T::kBBoxes; j += kWBlocks)
+            ptx::tma_load_3d_pair_hint(bdst + j * (kTileK * 128), &p.tmap_b, bar0, 0, b.brow + b.kb * kTileK,
+                                       b.n0 / 64 + j, b.pol);
     }
     ++b.issued;
     if (++b.stage == T::kStages) {

@@ -17,6 +17,7 @@ constexpr int kBlockRows = 128;    // row-block gate = GEMM M tile (section 5)
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 64;         // 64 bf16 = one 128-byte swizzle row
+constexpr int kWBlocks = 2;        // 64-column weight blocks per tensor load (one instruction)
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
 constexpr int kThreads = 512;      // 16 warps: TMA, MMA, 8 x epilogue, gate, 4 spare, stage waiter (consumers) / 16 copy warps (producers)
@@ -136,7 +137,8 @@ enum : int {
 
 struct FusedParams {
     CUtensorMap tmap_a;   // A: gathered / dispatched rows [rows][K] bf16, box 64 x 128, 128B swizzle
-    CUtensorMap tmap_b;   // B: weights [(E*)K][N] bf16 row-major (MN-major operand), box 64 x 64
+    CUtensorMap tmap_b;   // B: weights [(E*)K][N] bf16 row-major (MN-major operand) viewed as
+                          // [N/64][(E*)K][64], box 64 x 64 x kWBlocks (kWBlocks 64-column blocks per load)
     CUtensorMap tmap_out; // out [rows][N] bf16, box 32 x 32, 64B swizzle (rows past the extent are not stored)
     int mode;
     int M;                // gather: rows of the gathered buffer

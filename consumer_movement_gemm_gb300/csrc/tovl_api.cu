@@ -318,6 +318,25 @@ static int encode_2d(tovl_ctx* h, CUtensorMap* map, const void* base, uint64_t i
     return TOVL_OK;
 }
 
+// Weights W [rows][N] bf16 (N contiguous, N a multiple of 64) as a 3-D map
+// [N/64][rows][64]: one load brings kWBlocks 64-column blocks of 64 rows, in
+// the shared-memory layout of kWBlocks separate 64 x 64 boxes.
+static int encode_weights(tovl_ctx* h, CUtensorMap* map, const void* W, uint64_t N, uint64_t rows)
+{
+    cuuint64_t dims[3] = {64, rows, N / 64};
+    cuuint64_t strides[2] = {N * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(kWBlocks)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(h->last_error, sizeof h->last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+        return TOVL_ERR_INVALID;
+    }
+    return TOVL_OK;
+}
+
 // Waits inside one CTA's own pipeline depend on its gate waits, so their
 // bound must outlast a gate timeout.
 static long long pipe_timeout(const tovl_ctx* h)
@@ -519,7 +538,7 @@ static int run_gather(tovl_handle h, const void* const* shards, int S, int R, in
     int rc;
     if (flags & 2) {
         if ((rc = encode_2d(h, &p.tmap_a, A, K, M, static_cast<uint64_t>(K) * 2, kTileK, kTileM)) != TOVL_OK) return rc;
-        if ((rc = encode_2d(h, &p.tmap_b, W, N, K, static_cast<uint64_t>(N) * 2, 64, kTileK)) != TOVL_OK) return rc;
+        if ((rc = encode_weights(h, &p.tmap_b, W, N, K)) != TOVL_OK) return rc;
         if ((rc = encode_2d(h, &p.tmap_out, out, N, M, static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32,
                             CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
             return rc;
@@ -671,9 +690,7 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     int rc;
     if ((rc = encode_2d(h, &p.tmap_a, dispatched, H, rows, static_cast<uint64_t>(H) * 2, kTileK, kTileM)) != TOVL_OK)
         return rc;
-    if ((rc = encode_2d(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(N) * 2, 64, kTileK)) !=
-        TOVL_OK)
-        return rc;
+    if ((rc = encode_weights(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H)) != TOVL_OK) return rc;
     if ((rc = encode_2d(h, &p.tmap_out, out, N, rows, static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32,
                         CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
         return rc;
@@ -767,9 +784,7 @@ TOVL_API int tovl_gemm_reduce_scatter(tovl_handle h, const void* X, int num_shar
     if ((rc = encode_2d(h, &p.tmap_a, X, Ks, static_cast<uint64_t>(num_shards) * M, static_cast<uint64_t>(Ks) * 2,
                         kTileK, kTileM)) != TOVL_OK)
         return rc;
-    if ((rc = encode_2d(h, &p.tmap_b, W, N, static_cast<uint64_t>(num_shards) * Ks, static_cast<uint64_t>(N) * 2, 64,
-                        kTileK)) != TOVL_OK)
-        return rc;
+    if ((rc = encode_weights(h, &p.tmap_b, W, N, static_cast<uint64_t>(num_shards) * Ks)) != TOVL_OK) return rc;
     if ((rc = encode_2d(h, &p.tmap_out, partials, N, static_cast<uint64_t>(num_shards) * M,
                         static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
         return rc;
