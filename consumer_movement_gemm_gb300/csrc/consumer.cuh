@@ -1054,8 +1054,9 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
 }  // namespace dyn
 
 // Embedded producers: in a launch without producer CTAs, the consumer CTAs'
-// warps past the gate warp (5 per CTA) copy the rows, with the producers'
-// item order, counters and seeds (producer.cuh), dealt across every CTA.
+// warps between the gate warp and the stage waiter (4 per CTA) copy the
+// rows, with the producers' item order, counters and seeds (producer.cuh),
+// dealt across every CTA.
 // They own no mbarrier, TMEM column or ring entry, so they skip the
 // prologue: they count toward its barrier without waiting for it and start
 // as soon as the previous kernel's output (the plan) is visible.
