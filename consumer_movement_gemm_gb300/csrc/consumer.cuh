@@ -4,7 +4,8 @@
 // tiles in row-block order, the producers' order ("cross-GPU sync protocols
 // on PCIe", section 6 item 3).  Warp roles:
 //   warp 0      TMA: per tile and K-slice, waits for the slice's gate, then
-//               streams A (gathered rows) and B (weights) k-blocks into a
+//               streams A (gathered rows, one box per k-block) and B
+//               (weights, one 3-D box of kWBlocks 64-column blocks) into a
 //               ring of shared-memory stages
 //   warp 1      MMA: one lane issues tcgen05.mma into a double-buffered TMEM
 //               accumulator (2 x 256 fp32 columns)
