@@ -127,6 +127,26 @@ def test_gather_gemm_ragged(S, R, K, N, P, KS, pairs, mode):
             _check_ctrl(h, r)
 
 
+@pytest.mark.parametrize("S,R,K,N,KS", [(4, 96, 256, 512, 4), (3, 100, 192, 256, 2)])
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_gather_gemm_embedded_copy_warps(S, R, K, N, KS, pairs):
+    # option 18 = 2: the gather too runs without producer CTAs, its rows copied
+    # by the consumer CTAs' spare warps (the kernels with embedded producers,
+    # pair and single-CTA, in gather mode)
+    cfg = workloads.GatherCfg("embedded", S, R, K, N, rounds=3)
+    with _handle(k_slices=KS) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
+        h.set_option(tovl.OPT_EMBEDDED, 2)
+        for r in range(1, 4):
+            X, W, gathered, out = _gather_round(h, cfg, 200 + r)
+            assert h.sync_status() == 0
+            assert h.get_option(tovl.OPT_PRODUCERS) == 0
+            G = oracle.gather([bits(X[s]) for s in range(S)])
+            assert np.array_equal(bits(gathered), G)
+            assert_close(out, oracle.matmul_f32(G, bits(W)), "embedded gather")
+            _check_ctrl(h, r)
+
+
 @pytest.mark.parametrize("k_slices", [1, 4])
 def test_copy_only_control(k_slices):
     cfg = workloads.GatherCfg("copy", 4, 96, 256, 256, rounds=2)
@@ -649,12 +669,15 @@ def test_dispatch_pair_tiles_phantom_half_at_buffer_end():
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
-@pytest.mark.parametrize("align", [128, 256])
-def test_dispatch_embedded_producers(routing, align):
+@pytest.mark.parametrize("align,pairs", [(128, 1), (256, 1), (128, 0)])
+def test_dispatch_embedded_producers(routing, align, pairs):
     # option 18: no producer CTAs; the consumer CTAs' spare warps copy the
-    # rows; the same plan, buffers and counters as with producer CTAs
+    # rows; the same plan, buffers and counters as with producer CTAs.  With
+    # CTA pairs off the single-CTA kernel runs (its prologue barrier counts
+    # warps 0-10 and the stage waiter, not the copy warps)
     H, N = 192, 512
     with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_PAIRS, pairs)
         h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
         h.set_option(tovl.OPT_EMBEDDED, 1)
         assert h.get_option(tovl.OPT_EMBEDDED) == 1
