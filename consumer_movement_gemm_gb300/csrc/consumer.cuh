@@ -22,7 +22,11 @@
 // PAIR = 1: 128x256 tiles, stage = A 16 KB + B 32 KB, 4 stages.
 // PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
 // own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 5 stages beside
-// producer CTAs, 6 without); the
+// producer CTAs, 6 without).  A dispatch on the plan's pair table (embedded
+// producers) takes 256x512 tiles where N allows (NW = 2): two N = 256 MMAs
+// per k-step into one 512-column accumulator, each CTA staging A 16 KB and
+// 128 of each half's 256 columns (one 4-D weight box) per k-block, 4 stages;
+// the
 // pair's first CTA issues the MMAs, which read A and B halves from both CTAs
 // and accumulate each CTA's rows in its own TMEM.  Both CTAs' TMA loads are
 // counted on the first CTA's "full" barriers; MMA completion is multicast to
@@ -37,18 +41,23 @@
 
 namespace tovl {
 
-template <int PAIR, int ST = stages_for(PAIR)>
+// NW = 256-column MMAs per k-step: 1 for 256-column tiles (double-buffered
+// accumulator), 2 for 512-column CTA-pair tiles (one accumulator of all 512
+// TMEM columns; the weights as one 4-D box per k-block).
+template <int PAIR, int ST = stages_for(PAIR), int NW = 1>
 struct Tile {
     static constexpr int kStages = ST;
     static constexpr int kStageA = kTileM * kTileK * 2;               // 16 KB
-    static constexpr int kStageB = kTileK * kTileN * 2 / PAIR;        // this CTA's B columns
+    static constexpr int kStageB = kTileK * kTileN * NW * 2 / PAIR;   // this CTA's B columns
     static constexpr int kStageBytes = kStageA + kStageB;
-    static constexpr int kBBoxes = kTileN / 64 / PAIR;                // 64-column TMA boxes per stage
+    static constexpr int kBBoxes = kTileN * NW / 64 / PAIR;           // 64-column blocks per stage
+    static constexpr int kCols = kTileN * NW;                         // output columns of a tile
     // M = 128 * PAIR, N = 256, A K-major, B MN-major (W is [K][N], N contiguous)
     static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM * PAIR, kTileN, false, true);
-    static_assert(kStages * kStageBytes + kEpiWarps * kEpiBufBytes + 1024 <= smem_for(PAIR, ST),
+    static_assert(NW == 1 || PAIR == 2, "512-column tiles are CTA-pair tiles");
+    static_assert(kStages * kStageBytes + kEpiWarps * kEpiBufBytes * NW + 1024 <= smem_for(PAIR, ST, NW),
                   "stages and epilogue buffers must fit the dynamic shared memory");
-    static_assert(smem_for(PAIR, ST) <= 227 * 1024, "at most 227 KB of shared memory per CTA");
+    static_assert(smem_for(PAIR, ST, NW) <= 227 * 1024, "at most 227 KB of shared memory per CTA");
 };
 
 template <int PAIR>
@@ -70,15 +79,15 @@ struct ConsumerSmem {
 
 constexpr int kRing = 8;
 
-template <int PAIR, int ST = stages_for(PAIR)>
+template <int PAIR, int ST = stages_for(PAIR), int NW = 1>
 __device__ __forceinline__ ConsumerSmem<PAIR> consumer_smem(uint8_t* smem)
 {
-    using T = Tile<PAIR, ST>;
+    using T = Tile<PAIR, ST, NW>;
     ConsumerSmem<PAIR> s;
     s.a = smem;
     s.b = smem + T::kStages * T::kStageA;
     s.epi = smem + T::kStages * T::kStageBytes;   // 1024-byte aligned: stages are multiples of 1 KB
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + kEpiWarps * kEpiBufBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.epi + kEpiWarps * kEpiBufBytes * NW);
     s.full = bars;
     s.empty = bars + T::kStages;
     s.tfull = bars + 2 * T::kStages;
@@ -206,22 +215,22 @@ struct BCursor {
     uint64_t pol;             // L2 policy of the weight loads
 };
 
-template <int PAIR>
+template <int PAIR, int NW = 1>
 __device__ __forceinline__ void b_tile(const FusedParams& p, const Schedule<PAIR>& sc, BCursor<PAIR>& b)
 {
     if (b.t >= sc.n_tiles) return;
     const int mb = sc.expert_block(p, b.t);
     b.brow = (p.mode == kModeDispatch) ? p.blk_expert[mb] * p.K
            : (p.mode == kModeReduceScatter) ? sc.shard(p, b.t) * p.K : 0;
-    b.n0 = sc.col_block(p, b.t) * kTileN + static_cast<int>(sc.rank) * (kTileN / PAIR);
+    b.n0 = sc.col_block(p, b.t) * kTileN * NW + static_cast<int>(sc.rank) * (kTileN / PAIR);
 }
 
 // Arm the cursor's stage and issue its B boxes (the stage must be free).
-template <int PAIR, int ST>
+template <int PAIR, int ST, int NW = 1>
 __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                         BCursor<PAIR>& b)
 {
-    using T = Tile<PAIR, ST>;
+    using T = Tile<PAIR, ST, NW>;
     uint8_t* bdst = s.b + b.stage * T::kStageB;
     // one 3-D load per kWBlocks 64-column blocks (measured: each tensor-load
     // instruction stalls the MMA stream, two 2-D boxes per k-block cost 9.5
@@ -233,6 +242,14 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
         for (int j = 0; j < T::kBBoxes; j += kWBlocks)
             ptx::tma_load_3d_hint(bdst + j * (kTileK * 128), &p.tmap_b, &s.full[b.stage], 0, b.brow + b.kb * kTileK,
                                   b.n0 / 64 + j, b.pol);
+    } else if (NW == 2) {
+        // 512-column tiles: this CTA's 128 columns of each of the tile's two
+        // 256-column halves in one 4-D box ([N/256][4][rows][64] view, box
+        // 64 x 64 x 2 x 2): block z of half h lands h * 16 KB + z * 8 KB in
+        if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
+        const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&s.full[b.stage]), 0);
+        ptx::tma_load_4d_pair_hint(bdst, &p.tmap_b, bar0, 0, b.brow + b.kb * kTileK, (b.n0 % kTileN) / 64,
+                                   b.n0 / kTileN, b.pol);
     } else {
         // both CTAs' bytes are counted on the first CTA's barrier
         if (sc.rank == 0) ptx::mbar_arrive_expect_tx(&s.full[b.stage], PAIR * T::kStageBytes);
@@ -250,13 +267,13 @@ __device__ __forceinline__ void b_issue(const FusedParams& p, const ConsumerSmem
     if (++b.kb == p.n_kb) {
         b.kb = 0;
         b.t += sc.n_units;
-        b_tile<PAIR>(p, sc, b);
+        b_tile<PAIR, NW>(p, sc, b);
     }
 }
 
 // Arm stages until the cursor is `ahead` stages past `a_count` (blocking on
 // free stages only when `block`).  Returns false on a pipeline timeout.
-template <int PAIR, int ST>
+template <int PAIR, int ST, int NW = 1>
 __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                       BCursor<PAIR>& b, int upto, bool block)
 {
@@ -266,22 +283,22 @@ __device__ __forceinline__ bool b_run(const FusedParams& p, const ConsumerSmem<P
         } else if (!ptx::mbar_try_wait(&s.empty[b.stage], b.phase ^ 1u)) {
             return true;
         }
-        b_issue<PAIR, ST>(p, s, sc, b);
+        b_issue<PAIR, ST, NW>(p, s, sc, b);
     }
     return true;
 }
 
 // TMA lane: wait until the gate warp has passed gate number `idx` (bounded),
 // arming free stages with B meanwhile.
-template <int PAIR, int ST>
+template <int PAIR, int ST, int NW = 1>
 __device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                           BCursor<PAIR>& b, int a_count, int idx)
 {
-    using T = Tile<PAIR, ST>;
+    using T = Tile<PAIR, ST, NW>;
     if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
     const uint64_t start = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (!b_run<PAIR, ST>(p, s, sc, b, a_count + T::kStages, false)) return false;
+        if (!b_run<PAIR, ST, NW>(p, s, sc, b, a_count + T::kStages, false)) return false;
         if (ptx::ld_acquire_cta_smem(s.gates_passed) > idx) return true;
         if ((i & 63) == 0 && ptx::globaltimer() - start > static_cast<uint64_t>(p.pipe_timeout_ns)) {
             record_error(p.ctrl, kErrTimeout);
@@ -294,10 +311,10 @@ __device__ __forceinline__ bool wait_gate(const FusedParams& p, const ConsumerSm
 // TMA warp: per tile and K-slice, wait for the slice's gate, then stream the
 // slice's A k-blocks into stages whose B the cursor above has already
 // loaded.  One lane issues everything.
-template <int PAIR, int ST>
+template <int PAIR, int ST, int NW = 1>
 __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc)
 {
-    using T = Tile<PAIR, ST>;
+    using T = Tile<PAIR, ST, NW>;
     if (ptx::lane_id() != 0) return;
     BCursor<PAIR> b;
     b.t = sc.unit;
@@ -307,7 +324,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
     b.phase = 0;
     b.pol = stream_policy(p, kHintBLast, 0);
     const uint64_t pol_a = stream_policy(p, 0, kHintAFirst);
-    b_tile<PAIR>(p, sc, b);
+    b_tile<PAIR, NW>(p, sc, b);
     uint32_t stage = 0;
     int a_count = 0;
     int gate_idx = 0;
@@ -315,7 +332,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
         const int arow = sc.a_row(p, t);
         for (int sl = 0; sl < p.k_slices; ++sl, ++gate_idx) {
             if (p.gated) {
-                if (!wait_gate<PAIR, ST>(p, s, sc, b, a_count, gate_idx)) return;
+                if (!wait_gate<PAIR, ST, NW>(p, s, sc, b, a_count, gate_idx)) return;
                 // the rows were written through the generic proxy; order them
                 // before this thread's tensor-memory-access (async proxy) reads
                 ptx::fence_proxy_async_global();
@@ -323,7 +340,7 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
             const int kb1 = kb_begin(p, sl + 1);
             for (int kb = kb_begin(p, sl); kb < kb1; ++kb) {
                 // this k-block's stage is armed and holds (or receives) its B
-                if (!b_run<PAIR, ST>(p, s, sc, b, a_count + 1, true)) return;
+                if (!b_run<PAIR, ST, NW>(p, s, sc, b, a_count + 1, true)) return;
                 uint8_t* adst = s.a + stage * T::kStageA;
                 if (PAIR == 1) {
                     ptx::tma_load_2d_hint(adst, &p.tmap_a, &s.full[stage], kb * kTileK, arow, pol_a);
@@ -346,18 +363,19 @@ __device__ void consumer_tma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
 // MMAs over five rotating stages: 128.7 clocks per MMA with no waits, 139.0
 // with one already-complete wait per k-block; 141.5 in the full handshake
 // against 129.6 with the hand-off).
-template <int PAIR, int ST>
+template <int PAIR, int ST, int NW = 1>
 __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                              uint32_t tmem_base)
 {
-    using T = Tile<PAIR, ST>;
+    using T = Tile<PAIR, ST, NW>;
     if (sc.rank != 0) return;
     const bool lead = ptx::lane_id() == 0;
     uint32_t stage = 0;
     int local = 0;
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
-        const uint32_t acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
+        // two accumulators used in turn, or (512-column tiles) one
+        const uint32_t acc = NW == 1 ? (local & 1) : 0;
+        const uint32_t acc_phase = NW == 1 ? ((local >> 1) & 1) : (local & 1);
         if (lead) {
             // a timeout is recorded in the status word; the loop goes on, so
             // every stage hand-off of the waiter is still taken
@@ -382,9 +400,15 @@ __device__ void consumer_mma(const FusedParams& p, const ConsumerSmem<PAIR>& s, 
                     const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
                     // B: MN-major, 128B swizzle; +2048 B per 16 k-rows; 8-k-row
                     //    groups 1024 B apart; 64-column blocks 8 KB apart.
-                    const uint64_t bd = ptx::smem_desc_sw128(b0 + k * 2048, kTileK * 128, 1024);
-                    if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
-                    else ptx::umma_bf16_pair(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                    //    A 512-column tile's second half starts 16 KB in and
+                    //    accumulates into TMEM columns 256-511.
+#pragma unroll
+                    for (int h = 0; h < NW; ++h) {
+                        const uint64_t bd =
+                            ptx::smem_desc_sw128(b0 + h * (T::kStageB / NW) + k * 2048, kTileK * 128, 1024);
+                        if (PAIR == 1) ptx::umma_bf16(d, ad, bd, T::kIdesc, (kb | k) != 0);
+                        else ptx::umma_bf16_pair(d + h * kTileN, ad, bd, T::kIdesc, (kb | k) != 0);
+                    }
                 }
                 if (PAIR == 1) ptx::umma_commit(&s.empty[stage]);
                 else ptx::umma_commit_pair(&s.empty[stage], 0x3);
@@ -471,15 +495,20 @@ __device__ __forceinline__ void gstore_box(const FusedParams& p, uint32_t row_ad
 // few microseconds, and a tensor store holds its buffer for about a
 // microsecond).  The accumulator is released as soon as its last columns are
 // in registers.
-template <int PAIR>
+template <int PAIR, int NW = 1>
 __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>& s, const Schedule<PAIR>& sc,
                                   uint32_t tmem_base)
 {
+    // this warp's columns of a tile: half `half` of kCols, kBoxes boxes;
+    // 512-column tiles (an exposed drain: no second accumulator) stage their
+    // boxes in NW buffers used in turn
+    constexpr int kCols = kTileN * NW;
+    constexpr int kBoxes = kCols / 2 / kEpiBoxCols;
     const int warp = threadIdx.x / 32;
     const uint32_t lane = ptx::lane_id();
     const int q = warp & 3;
     const int half = (warp - kEpiWarp0) / 4;
-    const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes;
+    const uint8_t* buf = s.epi + (warp - kEpiWarp0) * kEpiBufBytes * NW;
     const uint32_t row_addr = ptx::smem_u32(buf) + lane * (kEpiBoxCols * 2);
     const uint32_t swz = (lane >> 1) & 3u;
     const uint64_t pol_out = stream_policy(p, 0, kHintOutFirst);
@@ -492,8 +521,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
     for (int t = sc.unit; t < sc.n_tiles; t += sc.n_units, ++local) {
         const int arow = sc.a_row(p, t);
         const int nb = sc.col_block(p, t);
-        const uint32_t acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
+        const uint32_t acc = NW == 1 ? (local & 1) : 0;
+        const uint32_t acc_phase = NW == 1 ? ((local >> 1) & 1) : (local & 1);
         const bool arrived = mbar_wait(&s.tfull[acc], acc_phase, p.ctrl, p.pipe_timeout_ns);
         if (!__all_sync(0xffffffffu, arrived)) break;
         ptx::tc_fence_after();
@@ -510,8 +539,8 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
             continue;
         }
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kTileN / 2);
-        if (gstore) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN + half * (kCols / 2);
+        if (NW == 1 && gstore) {
             // two boxes' accumulator loads in flight per wait
             const int col0 = nb * kTileN + half * (kTileN / 2);
 #pragma unroll
@@ -534,25 +563,19 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
             }
         }
 #pragma unroll 1
-        for (int bx = 0; bx < (gstore ? 0 : kTileN / 2 / kEpiBoxCols); ++bx) {
-            // the previous store from this buffer has finished reading it
-            if (lane == 0) ptx::bulk_wait_read<0>();
-            __syncwarp();
-            {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(taddr + bx * kEpiBoxCols, r);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint32_t chunk = static_cast<uint32_t>(v) ^ swz;
-                    ptx::st_shared_v4(row_addr + chunk * 16,
-                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
-                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                                      ptx::pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
-                }
+        for (int bx = 0; bx < ((NW == 1 && gstore) ? 0 : kBoxes); bx += NW) {
+            // NW boxes' accumulator columns per TMEM wait (512-column tiles:
+            // two), each box through its own staging buffer
+            uint32_t r[NW][32];
+            if (NW == 1) {
+                // the previous store from this buffer has finished reading it
+                if (lane == 0) ptx::bulk_wait_read<0>();
+                __syncwarp();
             }
-            if (bx == kTileN / 2 / kEpiBoxCols - 1) {
+#pragma unroll
+            for (int j = 0; j < NW; ++j) ptx::tmem_ld_32x32b_x32(taddr + (bx + j) * kEpiBoxCols, r[j]);
+            ptx::tmem_ld_wait();
+            if (bx + NW == kBoxes) {
                 // this warp's reads of the accumulator are done: one arrival per warp
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -561,13 +584,32 @@ __device__ void consumer_epilogue(const FusedParams& p, const ConsumerSmem<PAIR>
                     else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&s.tempty[acc]), 0));
                 }
             }
-            // the box's generic-proxy writes are visible to the tensor store
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::tma_store_2d_hint(&p.tmap_out, buf, nb * kTileN + half * (kTileN / 2) + bx * kEpiBoxCols,
-                                       arow + q * 32, pol_out);
-                ptx::bulk_commit();
+#pragma unroll
+            for (int j = 0; j < NW; ++j) {
+                const uint32_t jb = static_cast<uint32_t>(j) * kEpiBufBytes;
+                if (NW > 1) {
+                    // the store that last read buffer j (NW boxes ago) has finished reading it
+                    if (lane == 0) ptx::bulk_wait_read<NW - 1>();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t chunk = static_cast<uint32_t>(v) ^ swz;
+                    ptx::st_shared_v4(row_addr + jb + chunk * 16,
+                                      ptx::pack_bf16x2(__uint_as_float(r[j][8 * v + 0]), __uint_as_float(r[j][8 * v + 1])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[j][8 * v + 2]), __uint_as_float(r[j][8 * v + 3])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[j][8 * v + 4]), __uint_as_float(r[j][8 * v + 5])),
+                                      ptx::pack_bf16x2(__uint_as_float(r[j][8 * v + 6]), __uint_as_float(r[j][8 * v + 7])));
+                }
+                // the box's generic-proxy writes are visible to the tensor store
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d_hint(&p.tmap_out, buf + jb,
+                                           nb * kCols + half * (kCols / 2) + (bx + j) * kEpiBoxCols, arow + q * 32,
+                                           pol_out);
+                    ptx::bulk_commit();
+                }
             }
         }
         if (p.mode == kModeReduceScatter) {
@@ -1084,13 +1126,13 @@ __device__ __forceinline__ void embedded_producer(const FusedParams& p)
     if (PAIR == 2) ptx::cluster_wait();
 }
 
-template <int PAIR, bool DYN, bool EMB>
+template <int PAIR, bool DYN, bool EMB, int NW = 1>
 __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
 {
-    constexpr int ST = EMB ? emb_stages_for(PAIR) : stages_for(PAIR);
-    using T = Tile<PAIR, ST>;
+    constexpr int ST = NW == 2 ? kWideStages : (EMB ? emb_stages_for(PAIR) : stages_for(PAIR));
+    using T = Tile<PAIR, ST, NW>;
     const int warp = threadIdx.x / 32;
-    const ConsumerSmem<PAIR> s = consumer_smem<PAIR, ST>(smem);
+    const ConsumerSmem<PAIR> s = consumer_smem<PAIR, ST, NW>(smem);
     if (EMB && warp >= kFirstCopyWarp && warp < kWaitWarp) {
         embedded_producer<PAIR>(p);
         // the teardown barrier: TMEM is freed after every warp is done
@@ -1146,9 +1188,9 @@ __device__ void consumer(const FusedParams& p, uint8_t* smem, int cid)
         else if (warp < kEpiWarp0 + kEpiWarps) dyn::consumer_epilogue<PAIR, true>(p, s, sc, tmem_base);
         else if (warp == kGateWarp) dyn::consumer_gate<PAIR, true>(p, s, sc);
     } else {
-        if (warp == 0) consumer_tma<PAIR, ST>(p, s, sc);
-        else if (warp == 1) consumer_mma<PAIR, ST>(p, s, sc, tmem_base);
-        else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR>(p, s, sc, tmem_base);
+        if (warp == 0) consumer_tma<PAIR, ST, NW>(p, s, sc);
+        else if (warp == 1) consumer_mma<PAIR, ST, NW>(p, s, sc, tmem_base);
+        else if (warp < kEpiWarp0 + kEpiWarps) consumer_epilogue<PAIR, NW>(p, s, sc, tmem_base);
         else if (warp == kWaitWarp) consumer_stage_waiter<PAIR, ST>(p, s, sc);
         else if (warp == kGateWarp && p.gated) consumer_gate<PAIR>(p, s, sc);
         else if (warp >= kGateWarp && p.mode == kModeReduceScatter && p.rs_epi) {

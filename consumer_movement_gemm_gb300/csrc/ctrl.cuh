@@ -50,9 +50,10 @@ constexpr int kPairStages = 5;                     // pipeline stages of a CTA-p
 // memory is one its loads cannot have in flight, so the stages are as few as
 // keep the tensor pipe fed.
 constexpr int stages_for(int pair) { return pair == 1 ? kStages : kPairStages; }
-constexpr int smem_for(int pair, int stages)
+// (512-column tiles, nw = 2, give each epilogue warp two staging buffers)
+constexpr int smem_for(int pair, int stages, int nw = 1)
 {
-    return stages * (kStageA + kStageB / pair) + kEpiWarps * kEpiBufBytes + 1024 + 1024;
+    return stages * (kStageA + kStageB * nw / pair) + kEpiWarps * kEpiBufBytes * nw + 1024 + 1024;
 }
 constexpr int smem_bytes(int pair) { return smem_for(pair, stages_for(pair)); }
 // Launches without producer CTAs (embedded producers) leave no SM's L1 to
@@ -61,6 +62,10 @@ constexpr int smem_bytes(int pair) { return smem_for(pair, stages_for(pair)); }
 constexpr int kEmbPairStages = 6;
 constexpr int emb_stages_for(int pair) { return pair == 2 ? kEmbPairStages : stages_for(pair); }
 constexpr int smem_bytes_emb(int pair) { return smem_for(pair, emb_stages_for(pair)); }
+// 256 x 512 CTA-pair tiles (dispatch with embedded producers): each CTA
+// stages A 16 KB + 256 weight columns 32 KB per k-block, four stages.
+constexpr int kWideStages = 4;
+constexpr int smem_bytes_wide() { return smem_for(2, kWideStages, 2); }
 
 // Device status codes (mirror tovl.h).
 enum : int {
@@ -188,6 +193,7 @@ struct FusedParams {
     int dyn;              // consumer tiles handed out by a ticket counter (ctrl.work, zeroed by the plan kernel)
     int join;             // producer CTAs become consumers once their copies are done (role switch)
     int embedded;         // no producer CTAs: the consumer CTAs' spare warps copy the rows
+    int wide;             // CTA pairs compute 256 x 512 tiles (n_nb counts 512-column blocks; embedded dispatch)
     void* rs_out;         // [M][N] bf16
     // destinations
     void* gathered;       // gathered / dispatched buffer

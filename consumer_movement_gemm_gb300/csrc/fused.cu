@@ -35,7 +35,7 @@
 
 namespace tovl {
 
-template <int PAIR, bool DYN, bool EMB>
+template <int PAIR, bool DYN, bool EMB, int NW = 1>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ FusedParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         // takes GEMM tiles from the round's ticket counter like any consumer
         if (DYN && p.join) consumer<PAIR, DYN, false>(p, smem, -1);
     } else {
-        consumer<PAIR, DYN, EMB>(p, smem, blockIdx.x - p.n_producers);
+        consumer<PAIR, DYN, EMB, NW>(p, smem, blockIdx.x - p.n_producers);
     }
 }
 
@@ -58,7 +58,7 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(grid);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = p.embedded ? smem_bytes_emb(pair) : smem_bytes(pair);
+    lc.dynamicSmemBytes = p.wide ? smem_bytes_wide() : p.embedded ? smem_bytes_emb(pair) : smem_bytes(pair);
     lc.stream = stream;
     cudaLaunchAttribute attr[3];
     int n = 0;
@@ -81,6 +81,7 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t stream, bool coopera
     }
     lc.attrs = attr;
     lc.numAttrs = n;
+    if (p.wide) return cudaLaunchKernelEx(&lc, fused_kernel<2, false, true, 2>, p);
     if (p.embedded)
         return pair == 2 ? cudaLaunchKernelEx(&lc, fused_kernel<2, false, true>, p)
                          : cudaLaunchKernelEx(&lc, fused_kernel<1, false, true>, p);
@@ -103,6 +104,8 @@ cudaError_t prepare_fused()
         e = cudaFuncSetAttribute(fused_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_emb(1));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fused_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_emb(2));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<2, false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_wide());
     return e;
 }
 

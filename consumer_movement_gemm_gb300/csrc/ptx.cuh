@@ -476,6 +476,16 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(void* smem_dst, const CUte
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair_hint(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                      int x, int y, int z, int w, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint [%0], "
+        "[%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "r"(w), "l"(pol)
+        : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05 / TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols)
 {

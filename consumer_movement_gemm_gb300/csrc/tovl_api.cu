@@ -47,6 +47,7 @@ struct tovl_ctx {
     int role_switch = 1;       // 1: dispatch (single-CTA tiles) and reduce-scatter roles switch; 2: CTA-pair dispatch too
     int embedded = 1;          // without producer CTAs, the consumer CTAs' spare warps copy: 1 dispatch, 2 also gather
     int rs_epi = 0;            // 1: reduce-scatter tiles are summed by their owners' idle warps (no producer CTAs)
+    int wide_tiles = 1;        // 1: CTA-pair dispatch tiles (embedded producers) are 256 x 512 where N allows
     int l2_hints = -1;         // kHint* bits for every fused call; -1 = each call's measured default
     bool pdl_ok = true;        // cleared if the device rejects the launch attribute
     long long seq = 0;
@@ -337,6 +338,26 @@ static int encode_weights(tovl_ctx* h, CUtensorMap* map, const void* W, uint64_t
     return TOVL_OK;
 }
 
+// Weights for 256 x 512 CTA-pair tiles: the [rows][N] matrix viewed as
+// [N/256][4][rows][64] (64-column blocks grouped by 256-column half), box
+// 64 x 64 x 2 x 2: one load brings a CTA's 128 columns of both halves of a
+// 512-column tile for one k-block.
+static int encode_weights_wide(tovl_ctx* h, CUtensorMap* map, const void* W, uint64_t N, uint64_t rows)
+{
+    cuuint64_t dims[4] = {64, rows, kTileN / 64, N / kTileN};
+    cuuint64_t strides[3] = {N * 2, 128, kTileN * 2};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileK), 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(W), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(h->last_error, sizeof h->last_error, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+        return TOVL_ERR_INVALID;
+    }
+    return TOVL_OK;
+}
+
 // Waits inside one CTA's own pipeline depend on its gate waits, so their
 // bound must outlast a gate timeout.
 static long long pipe_timeout(const tovl_ctx* h)
@@ -616,6 +637,9 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     const bool pair_ok = h->pair_mode && h->max_pairs > 0;
     const bool pair_tab = pair_ok && align == kBlockRows && h->embedded != 0;
     const int pair = (pair_ok && (align == 2 * kBlockRows || pair_tab)) ? 2 : 1;
+    // pair-table tiles 512 columns wide: half the activation loads per MMA
+    // and one weight load per k-block for twice the MMAs
+    const bool wide = pair_tab && h->wide_tiles != 0 && N % (2 * kTileN) == 0;
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -649,7 +673,8 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     p.N = N;
     p.K = H;
     p.n_kb = H / kTileK;
-    p.n_nb = N / kTileN;
+    p.n_nb = N / (wide ? 2 * kTileN : kTileN);
+    p.wide = wide ? 1 : 0;
     p.row_bytes = H * 2;
     int P, C;
     // role switch: consumer tiles (single-CTA or CTA-pair) come from the
@@ -690,7 +715,9 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     int rc;
     if ((rc = encode_2d(h, &p.tmap_a, dispatched, H, rows, static_cast<uint64_t>(H) * 2, kTileK, kTileM)) != TOVL_OK)
         return rc;
-    if ((rc = encode_weights(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H)) != TOVL_OK) return rc;
+    rc = wide ? encode_weights_wide(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H)
+              : encode_weights(h, &p.tmap_b, W, N, static_cast<uint64_t>(E) * H);
+    if (rc != TOVL_OK) return rc;
     if ((rc = encode_2d(h, &p.tmap_out, out, N, rows, static_cast<uint64_t>(N) * 2, kEpiBoxCols, 32,
                         CU_TENSOR_MAP_SWIZZLE_64B)) != TOVL_OK)
         return rc;
@@ -1120,6 +1147,10 @@ TOVL_API int tovl_set_option(tovl_handle h, int option, long long value)
         if (value < -1 || value > 63) return TOVL_ERR_INVALID;
         h->l2_hints = static_cast<int>(value);
         return TOVL_OK;
+    case 23:
+        if (value != 0 && value != 1) return TOVL_ERR_INVALID;
+        h->wide_tiles = static_cast<int>(value);
+        return TOVL_OK;
     default:
         return TOVL_ERR_INVALID;
     }
@@ -1149,6 +1180,7 @@ TOVL_API int tovl_get_option(tovl_handle h, int option, long long* value)
     case 18: *value = h->embedded; return TOVL_OK;
     case 19: *value = h->rs_epi; return TOVL_OK;
     case 20: *value = h->l2_hints; return TOVL_OK;
+    case 23: *value = h->wide_tiles; return TOVL_OK;
     default: return TOVL_ERR_INVALID;
     }
 }

@@ -45,6 +45,7 @@ OPT_DISPATCH_ALIGN = 17
 OPT_EMBEDDED = 18
 OPT_RS_EPILOGUE = 19
 OPT_L2_HINTS = 20
+OPT_WIDE_TILES = 23
 
 
 class TovlError(RuntimeError):

@@ -353,6 +353,11 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * priorities; -1 (the default) = each call's measured choice: 32 | 8 for
  * tovl_gather_gemm, 8 for tovl_dispatch_grouped_gemm, 0 otherwise (results
  * are identical whatever the mask),
+ * 23 = tile width of tovl_dispatch_grouped_gemm's CTA-pair tiles on the
+ * plan's pair table (128-row segments, embedded producers): 1 (the default)
+ * = 256 x 512 tiles when N is a multiple of 512 (one 512-column accumulator,
+ * half the activation loads per MMA), else 256 x 256; 0 = always 256 x 256
+ * (results agree within the GEMM tolerance either way),
  * 8 = fault injection for tests: consumer gates
  * wait for sequence seq + value, which no producer publishes, so every gate
  * expires after the wait timeout and the call ends with TOVL_ERR_TIMEOUT in
@@ -373,7 +378,8 @@ int tovl_read_stats(tovl_handle h, unsigned long long* stats, int n);
  *   what 3: time each tile's accumulator was complete (epilogue start) [tiles]
  * Tiles are numbered row block * (N/256) + column block; for dispatch calls
  * the tile count is the bound tovl_dispatch_rows/128 * N/256 (unused tiles
- * read 0).  n must not exceed the stated length. */
+ * read 0), with 512-column pair tiles (option 23) N/512 column blocks.
+ * n must not exceed the stated length. */
 int tovl_read_trace(tovl_handle h, int what, long long* out, long long n);
 
 /* Publish and first-observe %globaltimer stamps of the first n chunks of the

@@ -669,6 +669,43 @@ def test_dispatch_pair_tiles_phantom_half_at_buffer_end():
 
 
 @pytest.mark.parametrize("routing", list(ROUTINGS))
+@pytest.mark.parametrize("H,N,KS", [(192, 512, 2), (320, 1536, 3), (1024, 1024, 1)])
+@pytest.mark.parametrize("wide", [1, 0])
+def test_dispatch_wide_pair_tiles(routing, H, N, KS, wide):
+    # option 23: CTA-pair tiles on the plan's pair table 512 columns wide (one
+    # 512-column accumulator, the weights as one 4-D box per k-block) or 256
+    # wide; N = 1536 gives three 512-column blocks, H = 320 five k-blocks
+    # over three K-slices; every routing has phantom halves
+    with _handle(k_slices=KS) as h:
+        h.set_option(tovl.OPT_WIDE_TILES, wide)
+        assert h.get_option(tovl.OPT_WIDE_TILES) == wide
+        for r in range(1, 4):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(6, r))
+            T = topk_np.shape[0]
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 400 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 410 + r, DEV)
+            dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+            assert h.sync_status() == 0
+            _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
+
+
+def test_dispatch_wide_pair_tiles_phantom_half_at_buffer_end():
+    # 512-column pair tiles whose second block is a phantom past the end of
+    # the buffer (two one-row experts fill rows = m_pad = 256)
+    H, N = 128, 512
+    with _handle(k_slices=2) as h:
+        assert h.get_option(tovl.OPT_WIDE_TILES) == 1
+        topk_np = np.array([[0], [1]], dtype=np.int32)
+        T, k = topk_np.shape
+        assert tovl.dispatch_rows(T, k, 2) == 256
+        x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 420, DEV)
+        W = workloads.bf16_normal((2, H, N), 1 / math.sqrt(H), 421, DEV)
+        dispatched, offs, out = _dispatch_round(h, x, topk_np, W)
+        assert h.sync_status() == 0
+        _check_dispatch(h, x, topk_np, W, dispatched, offs, out, 1)
+
+
+@pytest.mark.parametrize("routing", list(ROUTINGS))
 @pytest.mark.parametrize("align,pairs", [(128, 1), (256, 1), (128, 0)])
 def test_dispatch_embedded_producers(routing, align, pairs):
     # option 18: no producer CTAs; the consumer CTAs' spare warps copy the
