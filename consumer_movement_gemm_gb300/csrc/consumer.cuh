@@ -22,8 +22,8 @@
 // PAIR = 1: 128x256 tiles, stage = A 16 KB + B 32 KB, 4 stages.
 // PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
 // own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 5 stages beside
-// producer CTAs, 6 without).  A dispatch on the plan's pair table (embedded
-// producers) takes 256x512 tiles where N allows (NW = 2): two N = 256 MMAs
+// producer CTAs, 6 without).  A dispatch with embedded producers takes
+// 256x512 tiles where N allows (NW = 2): two N = 256 MMAs
 // per k-step into one 512-column accumulator, each CTA staging A 16 KB and
 // 128 of each half's 256 columns (one 4-D weight box) per k-block, 4 stages;
 // the

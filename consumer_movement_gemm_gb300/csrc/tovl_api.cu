@@ -637,9 +637,10 @@ TOVL_API int tovl_dispatch_grouped_gemm(tovl_handle h, const void* x, int T, int
     const bool pair_ok = h->pair_mode && h->max_pairs > 0;
     const bool pair_tab = pair_ok && align == kBlockRows && h->embedded != 0;
     const int pair = (pair_ok && (align == 2 * kBlockRows || pair_tab)) ? 2 : 1;
-    // pair-table tiles 512 columns wide: half the activation loads per MMA
-    // and one weight load per k-block for twice the MMAs
-    const bool wide = pair_tab && h->wide_tiles != 0 && N % (2 * kTileN) == 0;
+    // CTA-pair tiles of the embedded-producer kernel 512 columns wide: half
+    // the activation loads per MMA and one weight load per k-block for twice
+    // the MMAs
+    const bool wide = pair == 2 && h->embedded != 0 && h->wide_tiles != 0 && N % (2 * kTileN) == 0;
     DeviceGuard g(h->device);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
 

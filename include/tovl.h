@@ -353,8 +353,8 @@ int tovl_read_plan(tovl_handle h, int* counts, int* dst, int* src_of_dst, int* p
  * priorities; -1 (the default) = each call's measured choice: 32 | 8 for
  * tovl_gather_gemm, 8 for tovl_dispatch_grouped_gemm, 0 otherwise (results
  * are identical whatever the mask),
- * 23 = tile width of tovl_dispatch_grouped_gemm's CTA-pair tiles on the
- * plan's pair table (128-row segments, embedded producers): 1 (the default)
+ * 23 = tile width of tovl_dispatch_grouped_gemm's CTA-pair tiles with
+ * embedded producers (128- or 256-row segments): 1 (the default)
  * = 256 x 512 tiles when N is a multiple of 512 (one 512-column accumulator,
  * half the activation loads per MMA), else 256 x 256; 0 = always 256 x 256
  * (results agree within the GEMM tolerance either way),

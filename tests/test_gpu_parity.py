@@ -689,6 +689,36 @@ def test_dispatch_wide_pair_tiles(routing, H, N, KS, wide):
             _check_dispatch(h, x, topk_np, W, dispatched, offs, out, r)
 
 
+@pytest.mark.parametrize("routing", list(ROUTINGS))
+@pytest.mark.parametrize("wide", [1, 0])
+def test_dispatch_wide_pair_tiles_on_256_row_segments(routing, wide):
+    # option 17 = 256 with embedded producers: 256-row segments, CTA-pair
+    # tiles 512 (wide) or 256 columns wide, N = 1024
+    H, N, align = 256, 1024, 256
+    with _handle(k_slices=2) as h:
+        h.set_option(tovl.OPT_DISPATCH_ALIGN, align)
+        h.set_option(tovl.OPT_WIDE_TILES, wide)
+        for r in range(1, 3):
+            topk_np, E = ROUTINGS[routing](workloads.round_seed(8, r))
+            T, k = topk_np.shape
+            x = workloads.bf16_normal((T, H), 1 / math.sqrt(H), 430 + r, DEV)
+            W = workloads.bf16_normal((E, H, N), 1 / math.sqrt(H), 440 + r, DEV)
+            rows = tovl.dispatch_rows_aligned(T, k, E, align)
+            dispatched = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device=DEV)
+            offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+            out = torch.empty(rows, N, dtype=torch.bfloat16, device=DEV)
+            h.dispatch_grouped_gemm(x, torch.from_numpy(topk_np).to(DEV), W, dispatched, offs, out)
+            assert h.sync_status() == 0
+            p = oracle.dispatch_plan(topk_np, E, block_rows=align)
+            counts, dst, src, pad, blk, m_pad = h.read_plan(T, k, E)
+            assert m_pad == p.m_pad
+            assert np.array_equal(dst, p.dst)
+            D = oracle.dispatch(bits(x), p.dst, k, p.m_pad)
+            assert np.array_equal(bits(dispatched[:m_pad]), D), "dispatched buffer"
+            assert_close(out[:m_pad], oracle.grouped_matmul_f32(D, bits(W), p.off), f"256-row segments, wide {wide}")
+            _check_ctrl(h, r)
+
+
 def test_dispatch_wide_pair_tiles_phantom_half_at_buffer_end():
     # 512-column pair tiles whose second block is a phantom past the end of
     # the buffer (two one-row experts fill rows = m_pad = 256)
