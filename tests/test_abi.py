@@ -69,7 +69,7 @@ def test_new_entry_points_reject_null_handles(lib):
     assert L.tovl_combine(None, None, 0, None, None, None, None) == tovl.TOVL_ERR_INVALID
     assert L.tovl_gemm_reduce_scatter(None, None, 0, 0, 0, None, 0, None, None, None) == tovl.TOVL_ERR_INVALID
     v = ctypes.c_longlong()
-    for opt in (14, 15, 16, 17, 18):
+    for opt in (14, 15, 16, 17, 18, 19, 20, 23):
         assert L.tovl_set_option(None, opt, 0) == tovl.TOVL_ERR_INVALID
         assert L.tovl_get_option(None, opt, ctypes.byref(v)) == tovl.TOVL_ERR_INVALID
 

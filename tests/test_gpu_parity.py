@@ -719,6 +719,26 @@ def test_dispatch_wide_pair_tiles_on_256_row_segments(routing, wide):
             _check_ctrl(h, r)
 
 
+def test_option_ranges_are_checked():
+    # each documented option value round-trips; a value outside the
+    # documented range is rejected with TOVL_ERR_INVALID and leaves the
+    # option as it was
+    cases = {tovl.OPT_PDL: ([0, 1], [2, -1]), tovl.OPT_ROLE_SWITCH: ([0, 1, 2], [3, -1]),
+             tovl.OPT_DISPATCH_ALIGN: ([256, 128], [64, 192, 512]), tovl.OPT_EMBEDDED: ([0, 2, 1], [3, -1]),
+             tovl.OPT_RS_EPILOGUE: ([1, 0], [2, -1]), tovl.OPT_L2_HINTS: ([0, 63, -1], [64, -2]),
+             tovl.OPT_WIDE_TILES: ([0, 1], [2, -1])}
+    with _handle() as h:
+        for opt, (good, bad) in cases.items():
+            for v in good:
+                h.set_option(opt, v)
+                assert h.get_option(opt) == v
+            for v in bad:
+                with pytest.raises(tovl.TovlError) as e:
+                    h.set_option(opt, v)
+                assert e.value.code == tovl.TOVL_ERR_INVALID
+                assert h.get_option(opt) == good[-1]
+
+
 def test_dispatch_wide_pair_tiles_phantom_half_at_buffer_end():
     # 512-column pair tiles whose second block is a phantom past the end of
     # the buffer (two one-row experts fill rows = m_pad = 256)
