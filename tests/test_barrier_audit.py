@@ -82,7 +82,7 @@ def test_stage_handoff_barriers():
     consts = {k: int(v) for k, v in re.findall(r"constexpr int (k\w+) = (\d+);", ctrl)}
     assert consts["kStageBar0"] == 2 and consts["kStageBarThreads"] == 64
     assert consts["kWaitWarp"] == 15 and consts["kWaitWarp"] * 32 < consts["kThreads"]
-    most = max(consts["kStages"], consts["kPairStages"], consts["kEmbPairStages"])
+    most = max(consts["kStages"], consts["kPairStages"], consts["kEmbPairStages"], consts["kWideStages"])
     assert consts["kStageBar0"] + most <= 16
     for f in os.listdir(CSRC):
         if f == "ptx.cuh":
