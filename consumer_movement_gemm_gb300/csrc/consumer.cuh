@@ -23,12 +23,11 @@
 // PAIR = 2: 256x256 tiles per CTA pair (cta_group::2).  Each CTA stages its
 // own 128 rows of A and 128 of B's 256 columns (stage 32 KB, 5 stages beside
 // producer CTAs, 6 without).  A dispatch with embedded producers takes
-// 256x512 tiles where N allows (NW = 2): two N = 256 MMAs
-// per k-step into one 512-column accumulator, each CTA staging A 16 KB and
-// 128 of each half's 256 columns (one 4-D weight box) per k-block, 4 stages;
-// the
-// pair's first CTA issues the MMAs, which read A and B halves from both CTAs
-// and accumulate each CTA's rows in its own TMEM.  Both CTAs' TMA loads are
+// 256x512 tiles where N allows (NW = 2): two N = 256 MMAs per k-step into
+// one 512-column accumulator, each CTA staging A 16 KB and 128 of each
+// half's 256 columns (one 4-D weight box) per k-block, 4 stages.  The pair's
+// first CTA issues the MMAs, which read A and B halves from both CTAs and
+// accumulate each CTA's rows in its own TMEM.  Both CTAs' TMA loads are
 // counted on the first CTA's "full" barriers; MMA completion is multicast to
 // both CTAs; each CTA's epilogue warps release the accumulator on the first
 // CTA's "tmem empty" barrier.
